@@ -1,0 +1,178 @@
+"""Plain, slow fp64 CPU oracle of the Mixtral sparse-MoE feed-forward layer.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import it.  It
+shares no code with the CUDA library; the only thing both sides use is the
+seeded input generator in ``moe_workloads``.
+
+What it computes (per token t, independently), following the pages:
+
+  * "The Evolving Transformer - 05 Mixtral", section 05 (MoE router + MoE):
+    the layer output is the gate-weighted sum over the top-k experts,
+    y = sum_j w_j * E_{i_j}(x), with (w, i) from the router.
+  * Same page, section 05, class MoERouter: logits G(x) = x Wg^T (bias-free
+    linear d -> E), a softmax over all E logits, top-k of the probabilities
+    (sorted descending), then the k weights renormalised to sum to 1.
+  * Same page, section 04 (SwiGLU): each expert is three bias-free linear
+    maps, down(silu(gate(x)) * up(x)).  The tutorial names them w1 (gate),
+    w2 (up), w3 (down); this library names them W1 (gate), W3 (up), W2 (down).
+  * Same page, section 05, class MoE: the output starts at zero; for each
+    slot j and each expert e, the tokens whose slot-j expert is e are passed
+    through expert e and added with their slot-j weight.
+  * Same page, section 03 (RMSNorm) and section 06 (Block): the block form is
+    x + MoE(RMSNorm(x)) with RMSNorm(x) = x * (mean(x^2) + eps)^-1/2 * gamma.
+
+Readings where the pages are silent:
+  * Equal router probabilities keep the lower expert index first.
+  * In the block form the normalised activation is rounded once to bf16
+    (round to nearest even) before the router and the experts, as a bf16
+    layer stores it; everything else stays in fp64.
+
+Parity pins for every function here live in tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+try:  # torch tensors are accepted as inputs; the arithmetic is numpy fp64.
+    import torch
+except ImportError:  # pragma: no cover
+    torch = None
+
+
+def f64(a) -> np.ndarray:
+    """Exact fp64 copy of a numpy array or a CPU torch tensor (any float dtype)."""
+    if torch is not None and isinstance(a, torch.Tensor):
+        return a.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def round_to_bf16(v) -> np.ndarray:
+    """Round fp64 values to the nearest bfloat16 value, ties to even.
+
+    bfloat16 keeps 8 significant bits and fp32's exponent range; below the
+    smallest normal (2^-126) the spacing stays 2^-133.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)  # v = m * 2^e, 0.5 <= |m| < 1
+    e = np.maximum(e, -125)  # subnormal range: fixed spacing
+    scale = np.ldexp(1.0, 8 - e)  # spacing of 8-bit significands at this binade
+    return np.rint(v * scale) / scale  # np.rint rounds half to even
+
+
+# ---------------------------------------------------------------- RMSNorm
+def rmsnorm(x, gamma, eps) -> np.ndarray:
+    """Section 03 (RMSNorm): x * (mean over features of x^2 + eps)^-1/2 * gamma."""
+    x = f64(x)
+    g = f64(gamma)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * g
+
+
+# ---------------------------------------------------------------- router
+def router_logits(x, Wg) -> np.ndarray:
+    """Section 05, MoERouter: the bias-free gate, l[t, e] = sum_c x[t, c] Wg[e, c]."""
+    return f64(x) @ f64(Wg).T
+
+
+def softmax(l, axis=-1) -> np.ndarray:
+    z = l - np.max(l, axis=axis, keepdims=True)
+    p = np.exp(z)
+    return p / np.sum(p, axis=axis, keepdims=True)
+
+
+def router(x, Wg, k):
+    """Section 05, MoERouter.forward.
+
+    Returns (w[T,k], idx[T,k], logits[T,E]): softmax over all E logits, the k
+    largest probabilities in descending order (equal ones: lower index
+    first), and those k probabilities divided by their sum.
+    """
+    logits = router_logits(x, Wg)
+    prob = softmax(logits)
+    order = np.argsort(-prob, axis=-1, kind="stable")[:, :k]
+    w = np.take_along_axis(prob, order, axis=-1)
+    w = w / np.sum(w, axis=-1, keepdims=True)
+    return w, order.astype(np.int64), logits
+
+
+# ---------------------------------------------------------------- experts
+def silu(a) -> np.ndarray:
+    """SiLU (swish): a * sigmoid(a) = a / (1 + exp(-a))."""
+    return a / (1.0 + np.exp(-a))
+
+
+def swiglu_expert(x, W1e, W3e, W2e) -> np.ndarray:
+    """Section 04, SwiGLUFeedForward.forward: W2 (silu(W1 x) * (W3 x)).
+
+    x[n,d]; W1e, W3e [F,d] (gate, up); W2e [d,F] (down).  Returns [n,d].
+    """
+    x = f64(x)
+    a = x @ f64(W1e).T
+    b = x @ f64(W3e).T
+    h = silu(a) * b
+    return h @ f64(W2e).T
+
+
+# ---------------------------------------------------------------- layer
+def moe_forward_with_routing(x, W1, W3, W2, w, idx) -> np.ndarray:
+    """Section 05, MoE.forward given the router's (w, idx).
+
+    Output starts at zero; for each slot j, for each expert e, the tokens
+    whose slot-j expert is e go through expert e and are added with weight
+    w[:, j].  Experts that no token picked in a slot are skipped.
+    """
+    x = f64(x)
+    w = np.asarray(w, dtype=np.float64)
+    idx = np.asarray(idx)
+    T = x.shape[0]
+    E = W1.shape[0]
+    d = W2.shape[1]
+    out = np.zeros((T, d), dtype=np.float64)
+    for j in range(idx.shape[1]):
+        for e in range(E):
+            mask = idx[:, j] == e
+            if mask.any():
+                y = swiglu_expert(x[mask], W1[e], W3[e], W2[e])
+                out[mask] += w[mask, j][:, None] * y
+    return out
+
+
+def moe_forward(x, Wg, W1, W3, W2, k):
+    """The sparse MoE layer: returns (out[T,d], w[T,k], idx[T,k], logits[T,E])."""
+    w, idx, logits = router(x, Wg, k)
+    return moe_forward_with_routing(x, W1, W3, W2, w, idx), w, idx, logits
+
+
+def block_normed_input(x, gamma, eps) -> np.ndarray:
+    """Section 06 (Block), MoE half: the bf16-rounded RMSNorm(x) fed to the MoE."""
+    return round_to_bf16(rmsnorm(x, gamma, eps))
+
+
+def block_forward(x, gamma, eps, Wg, W1, W3, W2, k):
+    """Section 06 (Block), MoE half: x + MoE(RMSNorm(x)).
+
+    Returns (out[T,d], w, idx, logits, xn); logits and routing are those of
+    the normalised input xn.
+    """
+    xn = block_normed_input(x, gamma, eps)
+    delta, w, idx, logits = moe_forward(xn, Wg, W1, W3, W2, k)
+    return f64(x) + delta, w, idx, logits, xn
+
+
+# ---------------------------------------------------------------- shapes
+def expert_param_shapes(d, F):
+    """Shapes of one expert's three bias-free matrices: gate, up, down."""
+    return [(F, d), (F, d), (d, F)]
+
+
+def moe_layer_param_count(d, F, E) -> int:
+    """Parameters of one MoE layer: E experts plus the bias-free d->E gate."""
+    per_expert = sum(a * b for a, b in expert_param_shapes(d, F))
+    return E * per_expert + d * E
+
+
+def moe_layer_active_param_count(d, F, E, k) -> int:
+    """Parameters one token touches in an MoE layer: k experts and the gate."""
+    per_expert = sum(a * b for a, b in expert_param_shapes(d, F))
+    return k * per_expert + d * E

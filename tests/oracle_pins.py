@@ -1,0 +1,350 @@
+"""Checks that pin the fp64 oracle to facts other than itself.
+
+Each ``pin_*`` takes an oracle namespace ``o`` (the real ``oracle.moe_oracle``
+module, or a copy with a planted mistake) and raises on a mismatch.  The
+expected values come from brute force on tiny inputs, pure-Python textbook
+loops, closed forms, invariants of the layer, library routines for special
+cases, and the parameter counts printed on the pages — never from the
+oracle's own formulas retyped.
+
+Sources (page title, section):
+  * "The Evolving Transformer - 05 Mixtral", section 05 (MoE router + MoE),
+    section 04 (SwiGLU), section 03 (RMSNorm), section 06 (Block),
+    section 00 (Config).
+  * KerasFormers Mixtral docs, MixtralModel argument table.
+  * Mixtral 8x7B model reference page (46.7B total / 12.9B active).
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import mpmath
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+mpmath.mp.dps = 40
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _tiny_layer(seed, T=40, d=12, F=10, E=8, scale=1.0):
+    r = _rng(seed)
+    return dict(
+        x=r.standard_normal((T, d)) * scale,
+        Wg=r.standard_normal((E, d)) / math.sqrt(d),
+        W1=r.standard_normal((E, F, d)) / math.sqrt(d),
+        W3=r.standard_normal((E, F, d)) / math.sqrt(d),
+        W2=r.standard_normal((E, d, F)) / math.sqrt(F),
+    )
+
+
+def _py_dot(a, b):
+    return math.fsum(float(u) * float(v) for u, v in zip(a, b))
+
+
+def _py_silu(a):
+    return a / (1.0 + math.exp(-a))
+
+
+def _py_swiglu(xrow, W1e, W3e, W2e):
+    """Textbook SwiGLU for one token with pure-Python loops (gate W1, up W3, down W2)."""
+    F = len(W1e)
+    h = []
+    for f in range(F):
+        a = _py_dot(xrow, W1e[f])
+        b = _py_dot(xrow, W3e[f])
+        h.append(_py_silu(a) * b)
+    return [_py_dot(W2e[o], h) for o in range(len(W2e))]
+
+
+# ------------------------------------------------------------------ router
+def pin_router_logits_brute_force(o):
+    """Gate logits equal the per-(token, expert) dot product, summed exactly."""
+    L = _tiny_layer(1, T=6, d=7, E=5)
+    got = o.router_logits(L["x"], L["Wg"])
+    for t in range(6):
+        for e in range(5):
+            want = _py_dot(L["x"][t], L["Wg"][e])
+            assert abs(got[t, e] - want) <= 1e-13 * max(1.0, abs(want)), (t, e)
+
+
+def pin_topk_set_brute_force(o):
+    """The chosen set maximises the sum of logits over all C(E,k) subsets."""
+    for k in (1, 2, 3):
+        L = _tiny_layer(2 + k, T=60)
+        _, idx, _ = o.router(L["x"], L["Wg"], k)
+        logits = L["x"] @ L["Wg"].T  # exact enough: subsets differ by >> 1e-12 here
+        for t in range(60):
+            best = max(itertools.combinations(range(8), k), key=lambda s: sum(logits[t, list(s)]))
+            assert set(int(i) for i in idx[t]) == set(best), (k, t)
+
+
+def pin_slot_order_descending(o):
+    """Slot 0 carries the largest weight (top-k output is sorted)."""
+    L = _tiny_layer(7, T=80)
+    w, idx, _ = o.router(L["x"], L["Wg"], 3)
+    assert np.all(w[:, 0] >= w[:, 1]) and np.all(w[:, 1] >= w[:, 2])
+    logits = L["x"] @ L["Wg"].T
+    sel = np.take_along_axis(logits, idx, axis=1)
+    assert np.all(sel[:, 0] >= sel[:, 1]) and np.all(sel[:, 1] >= sel[:, 2])
+
+
+def pin_gate_weights_top2_sigmoid(o):
+    """k=2: renormalised softmax over the pair is sigmoid of the logit gap.
+
+    softmax(l)_i / (softmax(l)_i + softmax(l)_j) = 1 / (1 + exp(l_j - l_i)):
+    the normaliser over all E cancels.  Checked to 40 digits with mpmath.
+    """
+    L = _tiny_layer(11, T=50)
+    w, idx, _ = o.router(L["x"], L["Wg"], 2)
+    for t in range(50):
+        li = [mpmath.fsum(mpmath.mpf(float(a)) * mpmath.mpf(float(b)) for a, b in zip(L["x"][t], L["Wg"][e]))
+              for e in (int(idx[t, 0]), int(idx[t, 1]))]
+        w0 = 1 / (1 + mpmath.exp(li[1] - li[0]))
+        assert abs(w[t, 0] - float(w0)) < 1e-14, t
+        assert abs(w[t, 1] - float(1 - w0)) < 1e-14, t
+
+
+def pin_gate_weights_invariants(o):
+    """Weights are positive and sum to one for every k."""
+    for k in (1, 2, 4, 8):
+        L = _tiny_layer(13 + k, T=30)
+        w, _, _ = o.router(L["x"], L["Wg"], k)
+        assert np.all(w > 0)
+        assert np.allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+
+
+def pin_k1_weight_is_one(o):
+    """k=1: the single weight is exactly 1 and the layer is the argmax expert."""
+    L = _tiny_layer(17, T=20)
+    out, w, idx, _ = o.moe_forward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 1)
+    assert np.all(w == 1.0)
+    logits = L["x"] @ L["Wg"].T
+    for t in range(20):
+        e = int(np.argmax(logits[t]))
+        assert int(idx[t, 0]) == e
+        want = _py_swiglu(L["x"][t], L["W1"][e], L["W3"][e], L["W2"][e])
+        assert np.allclose(out[t], want, rtol=1e-12, atol=1e-14)
+
+
+def pin_equal_logits_split_evenly(o):
+    """Two identical, dominant gate rows: weights 0.5/0.5, lower index first."""
+    L = _tiny_layer(19, T=16)
+    Wg = L["Wg"].copy()
+    Wg[2] = Wg[5] = 1.0  # the same row twice
+    x = np.abs(L["x"]) + 0.5  # logits of rows 2/5 are the largest
+    w, idx, _ = o.router(x, Wg, 2)
+    assert np.all(idx[:, 0] == 2) and np.all(idx[:, 1] == 5)
+    assert np.all(w == 0.5)
+
+
+def pin_two_experts_select_both(o):
+    """E=2, k=2 selects both experts, larger logit first."""
+    L = _tiny_layer(23, T=25, E=2)
+    w, idx, _ = o.router(L["x"], L["Wg"], 2)
+    assert np.all(np.sort(idx, axis=1) == np.array([0, 1]))
+
+
+def pin_router_topk_softmax_restatement(o):
+    """Top-k of the logits, then a softmax over the k chosen (this library's
+    GPU formulation) equals softmax-over-all, top-k, renormalise."""
+    L = _tiny_layer(29, T=200)
+    for k in (2, 3):
+        w, idx, _ = o.router(L["x"], L["Wg"], k)
+        logits = L["x"] @ L["Wg"].T
+        for t in range(200):
+            order = sorted(range(8), key=lambda e: (-logits[t, e], e))[:k]
+            m = logits[t, order[0]]
+            ex = [math.exp(logits[t, e] - m) for e in order]
+            s = math.fsum(ex)
+            assert [int(i) for i in idx[t]] == order
+            assert np.allclose(w[t], [v / s for v in ex], rtol=0, atol=1e-14)
+
+
+# ------------------------------------------------------------------ experts
+def pin_silu_closed_form(o):
+    """silu(0)=0, silu(ln 3) = 0.75 ln 3, silu(-ln 3) = -0.25 ln 3."""
+    l3 = math.log(3.0)
+    got = o.silu(np.array([0.0, l3, -l3, 40.0]))
+    assert got[0] == 0.0
+    assert abs(got[1] - 0.75 * l3) < 1e-15
+    assert abs(got[2] + 0.25 * l3) < 1e-15
+    assert abs(got[3] - 40.0) < 1e-12
+
+
+def pin_swiglu_textbook(o):
+    """SwiGLU on 2 tokens x d=3 x F=4 against pure-Python loops."""
+    r = _rng(31)
+    x = r.standard_normal((2, 3))
+    W1, W3, W2 = r.standard_normal((4, 3)), r.standard_normal((4, 3)), r.standard_normal((3, 4))
+    got = o.swiglu_expert(x, W1, W3, W2)
+    for n in range(2):
+        assert np.allclose(got[n], _py_swiglu(x[n], W1, W3, W2), rtol=1e-13, atol=1e-15)
+
+
+def pin_swiglu_hand_values(o):
+    """A hand-worked SwiGLU: gate pre-activations ln 3 and 0, up 2 and 5.
+
+    x = [1, 0]; W1 rows give a = [ln 3, 0]; W3 rows give b = [2, 5];
+    h = [0.75 ln 3 * 2, 0 * 5] = [1.5 ln 3, 0]; W2 = [[1, 7], [-2, 3]]
+    gives y = [1.5 ln 3, -3 ln 3].
+    """
+    l3 = math.log(3.0)
+    x = np.array([[1.0, 0.0]])
+    W1 = np.array([[l3, 9.0], [0.0, -4.0]])
+    W3 = np.array([[2.0, 1.0], [5.0, 8.0]])
+    W2 = np.array([[1.0, 7.0], [-2.0, 3.0]])
+    y = o.swiglu_expert(x, W1, W3, W2)[0]
+    assert abs(y[0] - 1.5 * l3) < 1e-14 and abs(y[1] + 3.0 * l3) < 1e-14
+
+
+def pin_dense_reduction(o):
+    """E=1, k=1 is exactly the dense SwiGLU block of Mistral (section 04)."""
+    L = _tiny_layer(37, T=9, d=5, F=6, E=1)
+    out, w, idx, _ = o.moe_forward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 1)
+    assert np.all(idx == 0) and np.all(w == 1.0)
+    for t in range(9):
+        assert np.allclose(out[t], _py_swiglu(L["x"][t], L["W1"][0], L["W3"][0], L["W2"][0]),
+                           rtol=1e-12, atol=1e-14)
+
+
+def pin_identical_experts_reduce_to_one(o):
+    """All experts equal: any routing gives the single SwiGLU (weights sum to 1)."""
+    L = _tiny_layer(41, T=30, d=6, F=5)
+    for k in (2, 3):
+        W1 = np.repeat(L["W1"][:1], 8, axis=0)
+        W3 = np.repeat(L["W3"][:1], 8, axis=0)
+        W2 = np.repeat(L["W2"][:1], 8, axis=0)
+        out, _, _, _ = o.moe_forward(L["x"], L["Wg"], W1, W3, W2, k)
+        for t in range(30):
+            assert np.allclose(out[t], _py_swiglu(L["x"][t], W1[0], W3[0], W2[0]), rtol=1e-12, atol=1e-14)
+
+
+def pin_zero_input_zero_output(o):
+    L = _tiny_layer(43, T=5)
+    out, _, _, _ = o.moe_forward(np.zeros_like(L["x"]), L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    assert np.all(out == 0.0)
+
+
+def pin_down_projection_linear(o):
+    """Scaling every W2 by c scales the output by c; the routing does not move."""
+    L = _tiny_layer(47, T=40)
+    a, wa, ia, _ = o.moe_forward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    b, wb, ib, _ = o.moe_forward(L["x"], L["Wg"], L["W1"], L["W3"], -3.5 * L["W2"], 2)
+    assert np.array_equal(ia, ib) and np.array_equal(wa, wb)
+    assert np.allclose(b, -3.5 * a, rtol=1e-13, atol=1e-15)
+
+
+def pin_token_permutation_equivariance(o):
+    """Permuting the tokens permutes the output rows the same way."""
+    L = _tiny_layer(53, T=64)
+    perm = _rng(54).permutation(64)
+    a, _, _, _ = o.moe_forward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    b, _, _, _ = o.moe_forward(L["x"][perm], L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    assert np.allclose(b, a[perm], rtol=1e-13, atol=1e-15)
+
+
+def pin_layer_brute_force(o):
+    """Whole layer on tiny inputs: top-2 by brute force, weights by the sigmoid
+    form, experts by textbook loops, summed per token."""
+    L = _tiny_layer(59, T=12, d=6, F=5)
+    out, _, _, _ = o.moe_forward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    for t in range(12):
+        lg = [_py_dot(L["x"][t], L["Wg"][e]) for e in range(8)]
+        pair = max(itertools.combinations(range(8), 2), key=lambda s: lg[s[0]] + lg[s[1]])
+        i0, i1 = sorted(pair, key=lambda e: -lg[e])
+        w0 = 1.0 / (1.0 + math.exp(lg[i1] - lg[i0]))
+        y0 = _py_swiglu(L["x"][t], L["W1"][i0], L["W3"][i0], L["W2"][i0])
+        y1 = _py_swiglu(L["x"][t], L["W1"][i1], L["W3"][i1], L["W2"][i1])
+        want = [w0 * a + (1.0 - w0) * b for a, b in zip(y0, y1)]
+        assert np.allclose(out[t], want, rtol=1e-12, atol=1e-14), t
+
+
+# ------------------------------------------------------------------ norm / block
+def pin_rmsnorm_closed_form(o):
+    """Constant row c with gamma=1: every output is c / sqrt(c^2 + eps)."""
+    for c in (0.3, -2.0, 1e-3):
+        x = np.full((1, 16), c)
+        got = o.rmsnorm(x, np.ones(16), 1e-5)
+        assert np.allclose(got, c / math.sqrt(c * c + 1e-5), rtol=1e-15, atol=0)
+
+
+def pin_rmsnorm_mpmath(o):
+    """Random rows and gamma against a 40-digit evaluation of the definition."""
+    r = _rng(61)
+    x = r.standard_normal((3, 10))
+    g = 1.0 + 0.02 * r.standard_normal(10)
+    got = o.rmsnorm(x, g, 1e-5)
+    for t in range(3):
+        ms = mpmath.fsum(mpmath.mpf(float(v)) ** 2 for v in x[t]) / 10
+        inv = 1 / mpmath.sqrt(ms + mpmath.mpf(1e-5))
+        for c in range(10):
+            assert abs(got[t, c] - float(mpmath.mpf(float(x[t, c])) * inv * mpmath.mpf(float(g[c])))) < 1e-15
+
+
+def pin_round_to_bf16(o):
+    """fp64 -> bf16 rounding: hand ties, and torch's fp32 -> bf16 on fp32 inputs."""
+    one = 1.0
+    cases = {
+        one + 2.0 ** -8: 1.0,  # tie, keep even significand
+        one + 3 * 2.0 ** -8: one + 2.0 ** -6,  # tie, round up to even
+        one + 2.0 ** -8 + 2.0 ** -30: one + 2.0 ** -7,  # just above the tie
+        -(one + 2.0 ** -8): -1.0,
+        0.0: 0.0,
+    }
+    for v, want in cases.items():
+        assert o.round_to_bf16(np.array([v]))[0] == want, v
+    r = _rng(67)
+    v32 = (r.standard_normal(20000) * np.exp(r.uniform(-20, 20, 20000))).astype(np.float32)
+    want = torch.from_numpy(v32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(o.round_to_bf16(v32.astype(np.float64)), want)
+
+
+def pin_block_residual(o):
+    """gamma = 0 makes the normalised input zero, so the block returns x."""
+    L = _tiny_layer(71, T=10)
+    out, _, _, _, xn = o.block_forward(L["x"], np.zeros(12), 1e-5, L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    assert np.all(xn == 0.0)
+    assert np.array_equal(out, L["x"])
+
+
+def pin_block_uses_normalised_input(o):
+    """The block routes on RMSNorm(x): scaling a row by 8 (exact in binary)
+    leaves its routing unchanged when eps is negligible, and the MoE delta
+    is the layer applied to the bf16-rounded normalised row."""
+    L = _tiny_layer(73, T=20, scale=1.0)
+    g = np.ones(12)
+    a, _, ia, _, xa = o.block_forward(L["x"], g, 0.0, L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    b, _, ib, _, xb = o.block_forward(8.0 * L["x"], g, 0.0, L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    assert np.array_equal(ia, ib)
+    assert np.allclose(a - L["x"], b - 8.0 * L["x"], rtol=1e-12, atol=1e-12)
+    # every normalised value is a bf16 value
+    assert np.array_equal(xa, torch.from_numpy(xa).to(torch.bfloat16).to(torch.float64).numpy())
+
+
+# ------------------------------------------------------------------ shapes
+def pin_parameter_counts_match_pages(o):
+    """The 3-matrix bias-free SwiGLU experts at the pages' sizes reproduce the
+    pages' ~46.7B total and ~12.9B active parameters."""
+    with open(os.path.join(GOLDEN, "mixtral_8x7b_shapes.json")) as f:
+        g = {k: v["value"] for k, v in json.load(f).items() if not k.startswith("_")}
+    d, F, E, k, N = g["d_model"], g["d_ff"], g["num_experts"], g["top_k"], g["num_layers"]
+    head = d // g["num_heads"]
+    attn = 2 * d * d + 2 * d * (g["num_kv_heads"] * head)  # Wq, Wo; Wk, Wv
+    norms = 2 * d
+    emb = g["vocab_size"] * d * (1 if g["tie_embeddings"] else 2)
+    total = N * (o.moe_layer_param_count(d, F, E) + attn + norms) + emb + d
+    active = N * (o.moe_layer_active_param_count(d, F, E, k) + attn + norms) + emb + d
+    assert round(total / 1e9, 1) == g["total_params_billion_1dp"], total
+    assert round(active / 1e9, 1) == g["active_params_billion_1dp"], active
+    assert o.moe_layer_param_count(d, F, E) == 1_409_318_912
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,146 @@
+"""Plant plausible mistakes in a private copy of the oracle and check that at
+least one pin fails for each (CPU only; the real oracle is never modified).
+
+This shows the pins are strong enough: a dropped term, a wrong sign or index,
+a transposed operand or a swapped gate/up matrix cannot go unnoticed.
+"""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+from oracle_pins import ALL_PINS
+
+ORACLE_FILE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "moe_oracle.py")
+
+
+def fresh_oracle():
+    spec = importlib.util.spec_from_file_location("oracle_mutant", ORACLE_FILE)
+    m = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(m)
+    return m
+
+
+def _swap_gate_up(m):
+    orig = m.swiglu_expert
+    m.swiglu_expert = lambda x, W1e, W3e, W2e: orig(x, W3e, W1e, W2e)
+
+
+def _silu_sign(m):
+    m.silu = lambda a: a / (1.0 + np.exp(a))
+
+
+def _silu_is_sigmoid(m):
+    m.silu = lambda a: 1.0 / (1.0 + np.exp(-a))
+
+
+def _no_renormalise(m):
+    def router(x, Wg, k):
+        logits = m.router_logits(x, Wg)
+        prob = m.softmax(logits)
+        order = np.argsort(-prob, axis=-1, kind="stable")[:, :k]
+        return np.take_along_axis(prob, order, axis=-1), order, logits
+    m.router = router
+
+
+def _ascending_topk(m):
+    def router(x, Wg, k):
+        logits = m.router_logits(x, Wg)
+        prob = m.softmax(logits)
+        order = np.argsort(prob, axis=-1, kind="stable")[:, :k]
+        w = np.take_along_axis(prob, order, axis=-1)
+        return w / w.sum(-1, keepdims=True), order, logits
+    m.router = router
+
+
+def _ties_to_higher_index(m):
+    def router(x, Wg, k):
+        logits = m.router_logits(x, Wg)
+        prob = m.softmax(logits)
+        E = prob.shape[1]
+        order = (E - 1 - np.argsort(-prob[:, ::-1], axis=-1, kind="stable"))[:, :k]
+        w = np.take_along_axis(prob, order, axis=-1)
+        return w / w.sum(-1, keepdims=True), order, logits
+    m.router = router
+
+
+def _drop_gate_weight(m):
+    def fwd(x, W1, W3, W2, w, idx):
+        return m.__dict__["_orig_fwr"](x, W1, W3, W2, np.ones_like(np.asarray(w, dtype=float)), idx)
+    m._orig_fwr = m.moe_forward_with_routing
+    m.moe_forward_with_routing = fwd
+
+
+def _only_first_slot(m):
+    orig = m.moe_forward_with_routing
+    m.moe_forward_with_routing = lambda x, W1, W3, W2, w, idx: orig(x, W1, W3, W2, w[:, :1], idx[:, :1])
+
+
+def _transposed_down(m):
+    m.swiglu_expert = lambda x, W1e, W3e, W2e: (
+        m.silu(m.f64(x) @ m.f64(W1e).T) * (m.f64(x) @ m.f64(W3e).T)) @ m.f64(W2e)
+
+
+def _gate_transposed(m):
+    m.router_logits = lambda x, Wg: m.f64(x) @ m.f64(Wg)
+
+
+def _rms_no_square(m):
+    m.rmsnorm = lambda x, g, eps: m.f64(x) / np.sqrt(np.abs(np.mean(m.f64(x), -1, keepdims=True)) + eps) * m.f64(g)
+
+
+def _rms_no_eps(m):
+    m.rmsnorm = lambda x, g, eps: m.f64(x) / np.sqrt(np.mean(m.f64(x) ** 2, -1, keepdims=True)) * m.f64(g)
+
+
+def _rms_no_gamma(m):
+    m.rmsnorm = lambda x, g, eps: m.f64(x) / np.sqrt(np.mean(m.f64(x) ** 2, -1, keepdims=True) + eps)
+
+
+def _bf16_truncates(m):
+    def rnd(v):
+        v = np.asarray(v, dtype=np.float64)
+        mant, e = np.frexp(v)
+        s = np.ldexp(1.0, 8 - np.maximum(e, -125))
+        return np.trunc(v * s) / s
+    m.round_to_bf16 = rnd
+
+
+def _block_no_residual(m):
+    orig = m.block_forward
+    def blk(x, gamma, eps, Wg, W1, W3, W2, k):
+        out, w, idx, lg, xn = orig(x, gamma, eps, Wg, W1, W3, W2, k)
+        return out - m.f64(x), w, idx, lg, xn
+    m.block_forward = blk
+
+
+def _block_unnormalised(m):
+    def blk(x, gamma, eps, Wg, W1, W3, W2, k):
+        delta, w, idx, lg = m.moe_forward(m.f64(x), Wg, W1, W3, W2, k)
+        return m.f64(x) + delta, w, idx, lg, m.f64(x)
+    m.block_forward = blk
+
+
+def _two_matrix_expert(m):
+    m.expert_param_shapes = lambda d, F: [(F, d), (d, F)]
+
+
+MUTANTS = {f.__name__[1:]: f for f in [
+    _swap_gate_up, _silu_sign, _silu_is_sigmoid, _no_renormalise, _ascending_topk,
+    _ties_to_higher_index, _drop_gate_weight, _only_first_slot, _transposed_down,
+    _gate_transposed, _rms_no_square, _rms_no_eps, _rms_no_gamma, _bf16_truncates,
+    _block_no_residual, _block_unnormalised, _two_matrix_expert]}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name):
+    m = fresh_oracle()
+    MUTANTS[name](m)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(m)
+        except Exception:  # an assertion or a shape error both count
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name!r}"
