@@ -102,16 +102,42 @@ def silu(a) -> np.ndarray:
     return a / (1.0 + np.exp(-a))
 
 
+def swiglu_hidden(x, W1e, W3e) -> np.ndarray:
+    """Section 04, SwiGLUFeedForward: the hidden activation silu(W1 x) * (W3 x), [n,F]."""
+    x = f64(x)
+    a = x @ f64(W1e).T
+    b = x @ f64(W3e).T
+    return silu(a) * b
+
+
 def swiglu_expert(x, W1e, W3e, W2e) -> np.ndarray:
     """Section 04, SwiGLUFeedForward.forward: W2 (silu(W1 x) * (W3 x)).
 
     x[n,d]; W1e, W3e [F,d] (gate, up); W2e [d,F] (down).  Returns [n,d].
     """
-    x = f64(x)
-    a = x @ f64(W1e).T
-    b = x @ f64(W3e).T
-    h = silu(a) * b
-    return h @ f64(W2e).T
+    return swiglu_hidden(x, W1e, W3e) @ f64(W2e).T
+
+
+# ---------------------------------------------------------------- dispatch
+def dispatch(idx, E):
+    """Group the (token, slot) pairs by expert, as section 05's MoE loop does
+    when it selects the tokens routed to each expert.
+
+    The flat pair index is f = t*k + j.  Returns (counts[E], offsets[E+1],
+    row_src[T*k], slot_pos[T*k]): pairs sorted by expert with ties in
+    ascending f (a stable sort), row_src[p] the source token of row p, and
+    slot_pos[f] the row that pair f moved to.
+    """
+    idx = np.asarray(idx)
+    k = idx.shape[1]
+    flat = idx.reshape(-1)
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    order = np.argsort(flat, kind="stable")  # order[p] = pair at row p
+    row_src = order // k
+    slot_pos = np.empty_like(order)
+    slot_pos[order] = np.arange(order.size)
+    return counts, offsets, row_src, slot_pos
 
 
 # ---------------------------------------------------------------- layer

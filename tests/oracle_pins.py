@@ -168,6 +168,37 @@ def pin_router_topk_softmax_restatement(o):
             assert np.allclose(w[t], [v / s for v in ex], rtol=0, atol=1e-14)
 
 
+def pin_dispatch_brute_force(o):
+    """Rows grouped per expert in ascending (token, slot), by plain loops."""
+    r = _rng(5)
+    for k, E, T in ((2, 8, 37), (1, 3, 10), (3, 5, 0), (2, 8, 1)):
+        idx = np.stack([r.permutation(E)[:k] for _ in range(T)]) if T else np.zeros((0, k), dtype=np.int64)
+        counts, offsets, row_src, slot_pos = o.dispatch(idx, E)
+        rows = []
+        for e in range(E):
+            for t in range(T):
+                for j in range(k):
+                    if idx[t, j] == e:
+                        rows.append((t, j))
+        assert list(counts) == [sum(1 for t in range(T) for j in range(k) if idx[t, j] == e) for e in range(E)]
+        assert list(offsets) == [sum(counts[:e]) for e in range(E + 1)]
+        assert [int(v) for v in row_src] == [t for t, _ in rows]
+        for p, (t, j) in enumerate(rows):
+            assert slot_pos[t * k + j] == p
+
+
+def pin_swiglu_hidden_textbook(o):
+    """The hidden activation silu(W1 x) * (W3 x) by pure-Python loops."""
+    r = _rng(33)
+    x = r.standard_normal((3, 4))
+    W1, W3 = r.standard_normal((5, 4)), r.standard_normal((5, 4))
+    got = o.swiglu_hidden(x, W1, W3)
+    for n in range(3):
+        for f in range(5):
+            want = _py_silu(_py_dot(x[n], W1[f])) * _py_dot(x[n], W3[f])
+            assert abs(got[n, f] - want) < 1e-13 * max(1.0, abs(want))
+
+
 # ------------------------------------------------------------------ experts
 def pin_silu_closed_form(o):
     """silu(0)=0, silu(ln 3) = 0.75 ln 3, silu(-ln 3) = -0.25 ln 3."""

@@ -122,6 +122,31 @@ def _block_unnormalised(m):
     m.block_forward = blk
 
 
+def _dispatch_unstable(m):
+    orig = m.dispatch
+    def disp(idx, E):
+        counts, offsets, row_src, slot_pos = orig(idx, E)
+        return counts, offsets, row_src[::-1].copy(), slot_pos
+    m.dispatch = disp
+
+
+def _dispatch_token_not_pair(m):
+    def disp(idx, E):
+        idx = np.asarray(idx)
+        flat = idx.reshape(-1)
+        counts = np.bincount(flat, minlength=E)
+        offsets = np.concatenate([[0], np.cumsum(counts)])
+        order = np.argsort(flat, kind="stable")
+        slot_pos = np.empty_like(order)
+        slot_pos[order] = np.arange(order.size)
+        return counts, offsets, order, slot_pos  # pair index instead of token
+    m.dispatch = disp
+
+
+def _hidden_no_gate(m):
+    m.swiglu_hidden = lambda x, W1e, W3e: m.f64(x) @ m.f64(W3e).T
+
+
 def _two_matrix_expert(m):
     m.expert_param_shapes = lambda d, F: [(F, d), (d, F)]
 
@@ -130,7 +155,8 @@ MUTANTS = {f.__name__[1:]: f for f in [
     _swap_gate_up, _silu_sign, _silu_is_sigmoid, _no_renormalise, _ascending_topk,
     _ties_to_higher_index, _drop_gate_weight, _only_first_slot, _transposed_down,
     _gate_transposed, _rms_no_square, _rms_no_eps, _rms_no_gamma, _bf16_truncates,
-    _block_no_residual, _block_unnormalised, _two_matrix_expert]}
+    _block_no_residual, _block_unnormalised, _two_matrix_expert, _dispatch_unstable,
+    _dispatch_token_not_pair, _hidden_no_gate]}
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
