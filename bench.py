@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the B300 Mixtral sparse-MoE layer (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                    [--workloads decode,prefill,...] [--no-cpu-baseline]
+
+A step is one pass of the whole hot path - router, dispatch, grouped gate/up
+GEMM with SwiGLU, grouped down GEMM, combine (and the RMSNorm prologue and
+residual for the block workload) - over one batch of synthetic tokens, run
+through the library's C ABI with every input already in HBM.  The headline
+workload is Mixtral-shape decode (T=16); the other Mixtral workloads are
+timed in the same run and reported under "workloads".
+
+Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA
+events on the launching stream, with an L2 flush (a 256 MiB write) between
+steps outside the events; a barrier and a device synchronise on both sides.
+Per-kernel events inside the step give the dominant kernel's roofline.
+"e2e" runs moe_forward_host with pinned host activations (host->device copy,
+the layer, device->host copy, synchronise) timed by the host clock.
+
+Multi-GPU (torchrun): replicas only - every rank runs the same workload on its
+own GPU with no collective on the data path; value = tokens of all ranks /
+max over ranks of the timed region.  ``--impl reference`` times the fp64 CPU
+oracle on the host cores (rank 0 only) on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import moe_workloads as mw  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (Mixtral 4096/14336, E8 k2, bf16) + % of roofline"
+HEADLINE = "decode"
+ALL_BENCH = ["decode", "prefill", "skewed", "skewed_zero", "block"]
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = {False: 6, True: 7}  # router, rank, gather, gate_up, down, combine (+ rmsnorm)
+
+
+# ---------------------------------------------------------------- peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- work model
+def algorithmic(wl, counts):
+    """Algorithmic FLOPs and bytes of one layer call, and of its gate/up GEMM.
+
+    FLOP/token = k*6*d*F + 2*d*E.  Bytes = every used expert's three matrices
+    + the gate + x in + out (+ gamma); permuted intermediates do not count.
+    """
+    T, d, F, E, k = wl.T, wl.d, wl.F, wl.E, wl.k
+    used = int(sum(1 for c in counts if c > 0))
+    flops = T * (k * 6 * d * F + 2 * d * E)
+    nbytes = used * 3 * d * F * 2 + d * E * 2 + 2 * T * d * 2 + (d * 2 if wl.block else 0)
+    gu_flops = T * k * 4 * d * F
+    gu_bytes = used * 2 * d * F * 2
+    return flops, nbytes, gu_flops, gu_bytes
+
+
+# ---------------------------------------------------------------- ncu traffic
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("ffn_tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "sparse_mixture_experts_50_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per gate/up launch from a committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"gate_up_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch_full:\s*([0-9.e+]+)", text)
+    if not (m_src and m_b) or m_src.group(1) != kernel_source_hash():
+        return None
+    return float(m_b.group(1))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the layer
+class Layer:
+    """Device-resident inputs and buffers of one workload.  step() runs the
+    whole hot path through the C ABI; with `ev` (5 CUDA events) it records
+    them before the router, after dispatch, after gate/up, after down and
+    after combine."""
+
+    def __init__(self, wl, tensors, device):
+        from sparse_mixture_experts_50_b300 import binding as B
+        self.B = B
+        self.wl = wl
+        T, d, F, E, k = wl.T, wl.d, wl.F, wl.E, wl.k
+        dev = torch.device(device)
+        g = {n: v.to(dev, non_blocking=False) for n, v in tensors.items()}
+        self.x, self.Wg, self.W1, self.W3, self.W2 = g["x"], g["Wg"], g["W1"], g["W3"], g["W2"]
+        self.gamma = g.get("gamma")
+        dt = wl.torch_dtype
+        self.xn = torch.empty((T, d), dtype=dt, device=dev) if wl.block else None
+        self.idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.counts = torch.empty(E, dtype=torch.int32, device=dev)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        self.row_src = torch.empty(T * k, dtype=torch.int32, device=dev)
+        self.slot_pos = torch.empty(T * k, dtype=torch.int32, device=dev)
+        self.x_perm = torch.empty((T * k, d), dtype=dt, device=dev)
+        self.h = torch.empty((T * k, F), dtype=dt, device=dev)
+        self.y = torch.empty((T * k, d), dtype=dt, device=dev)
+        self.out = torch.empty((T, d), dtype=dt, device=dev)
+
+    def step(self, ev=None):
+        B, wl = self.B, self.wl
+        if ev is not None:
+            ev[0].record()
+        xin = self.x
+        if self.gamma is not None:
+            B.moe_rmsnorm(self.x, self.gamma, wl.eps, xn=self.xn)
+            xin = self.xn
+        B.moe_router_topk(xin, self.Wg, wl.k, self.idx, self.w)
+        B.moe_permute(xin, self.idx, wl.E, out=(self.counts, self.offsets, self.row_src, self.slot_pos, self.x_perm))
+        if ev is not None:
+            ev[1].record()
+        B.moe_expert_gate_up(self.x_perm, self.offsets, self.W1, self.W3, self.h)
+        if ev is not None:
+            ev[2].record()
+        B.moe_expert_down(self.h, self.offsets, self.W2, self.y)
+        if ev is not None:
+            ev[3].record()
+        B.moe_combine(self.y, self.slot_pos, self.w, wl.T, residual=self.x if wl.block else None, out=self.out)
+        if ev is not None:
+            ev[4].record()
+        return self.out
+
+
+def make_tensors(wl, shared):
+    """CPU tensors of a workload; the expert weights (which do not depend on
+    T or the gate bias) are drawn once and shared across workloads."""
+    key = (wl.d, wl.F, wl.E, wl.dtype, wl.init)
+    if key not in shared:
+        shared[key] = mw.make_inputs(wl, only=("W1", "W3", "W2"))
+    rest = mw.make_inputs(wl, only=("x", "Wg", "gamma"))
+    return {**rest, **shared[key]}
+
+
+def time_layer(layer, steps, warmup, flush, dist_on):
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for _ in range(warmup):
+        layer.step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        layer.step(evs[i])
+        flush.zero_()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    parts = {
+        "router_dispatch": [e[0].elapsed_time(e[1]) for e in evs],
+        "gate_up": [e[1].elapsed_time(e[2]) for e in evs],
+        "down": [e[2].elapsed_time(e[3]) for e in evs],
+        "combine": [e[3].elapsed_time(e[4]) for e in evs],
+    }
+    return step_ms, parts, wall
+
+
+def bench_workload(name, shared, args, device, peaks, dist_on):
+    wl = mw.get(name)
+    layer = Layer(wl, make_tensors(wl, shared), device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    layer.step()
+    status = layer.B.moe_get_device_status(reset=True)
+    if status != 0:
+        raise RuntimeError(f"{name}: device status {status} after the first step")
+    counts = layer.counts.cpu().tolist()
+    step_ms, parts, wall = time_layer(layer, args.steps, args.warmup, flush, dist_on)
+    status = layer.B.moe_get_device_status(reset=True)
+    if status != 0:
+        raise RuntimeError(f"{name}: device status {status} after the timed steps")
+    ms = sum(step_ms) / len(step_ms)
+    flops, nbytes, gu_flops, gu_bytes = algorithmic(wl, counts)
+    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    bound = "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor"
+    gu_ms = sum(parts["gate_up"]) / len(parts["gate_up"])
+    if bound == "hbm":
+        achieved, peak, unit = gu_bytes / (gu_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = gu_flops / (gu_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    res = {
+        "workload": name, "T": wl.T, "tokens_per_s": wl.T / (ms * 1e-3), "ms_per_step": ms,
+        "layer_roofline_frac": t_roof / (ms * 1e-3), "bound": bound,
+        "layer_roofline_tokens_per_s": wl.T / t_roof,
+        "kernel_ms": {p: sum(v) / len(v) for p, v in parts.items()},
+        "expert_counts": counts,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "kernel": "grouped_gemm_tc_kernel<gate_up+SwiGLU>",
+                     "algorithmic_per_launch": gu_bytes if bound == "hbm" else gu_flops,
+                     "traffic": ncu_traffic(name)},
+        "wall_s": wall,
+    }
+    return res, layer
+
+
+def e2e_leg(layer, steps, warmup):
+    """moe_forward_host with pinned host activations, host-clock timed."""
+    B, wl = layer.B, layer.wl
+    x_host = layer.x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    ws = B.workspace(wl.T, wl.d, wl.F, wl.E, wl.k, B.MOE_DTYPE_BF16, device=layer.x.device, host=True)
+    for _ in range(warmup):
+        B.moe_forward_host(x_host, layer.Wg, layer.W1, layer.W3, layer.W2, wl.k, ws, out_host)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        B.moe_forward_host(x_host, layer.Wg, layer.W1, layer.W3, layer.W2, wl.k, ws, out_host)
+    el = time.perf_counter() - t0
+    nb = wl.T * wl.d * 2
+    return {"value": wl.T * steps / el, "unit": "tokens/s", "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb}
+
+
+def oracle_sample(name, max_tokens=None):
+    """Time the fp64 CPU oracle on a bounded sample of the workload."""
+    import oracle.moe_oracle as O
+    wl = mw.get(name)
+    t = mw.make_inputs(wl)
+    n = wl.T if max_tokens is None else min(wl.T, max_tokens)
+    x = t["x"][:n]
+    t0 = time.perf_counter()
+    if wl.block:
+        O.block_forward(x, t["gamma"], wl.eps, t["Wg"], t["W1"], t["W3"], t["W2"], wl.k)
+    else:
+        O.moe_forward(x, t["Wg"], t["W1"], t["W3"], t["W2"], wl.k)
+    el = time.perf_counter() - t0
+    try:
+        import threadpoolctl
+        cores = max((i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()), default=1)
+    except Exception:  # pragma: no cover
+        cores = os.cpu_count()
+    return {"value": n / el, "unit": "tokens/s", "cores": int(cores), "kind": "oracle",
+            "sample": f"{name}: first {n} of {wl.T} tokens, full layer in fp64 (numpy), {el:.1f} s"}
+
+
+def config_of(name, n_gpus):
+    wl = mw.get(name)
+    return {"workload": f"{name}: T={wl.T}, d={wl.d}, d_ff={wl.F}, E={wl.E}, top-{wl.k}, {wl.dtype}"
+                        + (", RMSNorm + residual" if wl.block else "")
+                        + (", skewed expert load" if wl.skew else ""),
+            "T": wl.T, "d": wl.d, "d_ff": wl.F, "E": wl.E, "k": wl.k,
+            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
+            "l2": "flushed between timed steps (256 MiB write); expert weights (2.8 GB) also exceed L2"}
+
+
+def ensure_built():
+    from sparse_mixture_experts_50_b300 import binding
+    if not os.path.exists(binding.LIB_PATH):
+        from sparse_mixture_experts_50_b300.build import build
+        build()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workloads", default=",".join(ALL_BENCH))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    names = [n for n in args.workloads.split(",") if n]
+    if HEADLINE not in names:
+        names.insert(0, HEADLINE)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        t0 = time.perf_counter()
+        samples = []
+        for _ in range(args.warmup):
+            pass  # the oracle has no warm-up state; each step is a fresh evaluation
+        for _ in range(max(1, min(args.steps, 3))):
+            samples.append(oracle_sample(HEADLINE))
+        v = statistics.median(s["value"] for s in samples)
+        line = {"metric": METRIC, "value": v, "unit": "tokens/s", "impl": "reference", "n_gpus": 1,
+                "steps": len(samples), "warmup": args.warmup, "ms_per_step": 1e3 * mw.get(HEADLINE).T / v,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config_of(HEADLINE, 1),
+                "cpu_baseline": {**samples[0], "value": v},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": time.perf_counter() - t0}
+        print(json.dumps(line), flush=True)
+        return
+
+    dist_on = world > 1
+    if dist_on:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the native implementation")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    ensure_built()
+    peaks = load_peaks()
+    shared = {}
+    clocks = ClockSampler(local)
+    results = {}
+    head_layer = None
+    for name in names:
+        if name == HEADLINE:
+            clocks.start()
+        res, layer = bench_workload(name, shared, args, device, peaks, dist_on)
+        if name == HEADLINE:
+            res["clocks"] = clocks.stop()
+            head_layer = layer
+        else:
+            del layer
+        results[name] = res
+        torch.cuda.empty_cache()
+
+    head = results[HEADLINE]
+    # Whole job: tokens of all ranks over the slowest rank's timed region.
+    t_local = head["ms_per_step"] * args.steps * 1e-3
+    t_max = t_local
+    if dist_on:
+        tt = torch.tensor([t_local], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(tt.item())
+    value = world * mw.get(HEADLINE).T * args.steps / t_max
+
+    e2e = None if args.no_e2e else e2e_leg(head_layer, args.steps, args.warmup)
+    if dist_on and e2e is not None:
+        tt = torch.tensor([e2e["value"]], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MIN)
+        e2e["value"] = float(tt.item()) * world
+
+    if rank == 0:
+        cpu = None if (args.no_cpu_baseline or dist_on) else oracle_sample(HEADLINE)
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(HEADLINE, world), "impl": "native",
+            "roofline": {k: head["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
+            "roofline_detail": {**head["roofline"], "peak_source": peaks["source"],
+                                "layer_frac": head["layer_roofline_frac"]},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP[mw.get(HEADLINE).block] * args.steps,
+            "clocks": head.get("clocks"),
+            "workloads": {n: {k: v for k, v in r.items() if k not in ("clocks",)} for n, r in results.items()},
+        }
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+/*
+ * moe.h - C ABI of libmoe, the B300 (sm_103a) Mixtral sparse mixture-of-experts
+ * feed-forward layer.
+ *
+ * The layer (page "The Evolving Transformer - 05 Mixtral", section 05, the
+ * formula y = sum_j w_j * E_{i_j}(x) and classes MoERouter / MoE):
+ *   logits  l = x Wg^T                         (bias-free gate, d -> E)
+ *   (i, w)  = top-k of l, softmax over those k  (= softmax over all E, top-k,
+ *                                               renormalise over the k chosen)
+ *   E_e(x)  = W2_e (silu(W1_e x) * (W3_e x))    (section 04, SwiGLU; W1 gate,
+ *                                               W3 up, W2 down)
+ *   out[t]  = sum_j w[t,j] E_{i[t,j]}(x[t])
+ * Block form (section 06, Block; section 03, RMSNorm):
+ *   out = x + MoE(RMSNorm(x)),  RMSNorm(x) = x (mean(x^2) + eps)^-1/2 gamma.
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller, unless a
+ *    parameter says "host".  The library never frees or keeps them.
+ *  - Row-major layouts; every operand is contiguous along its last index:
+ *      x[T,d], Wg[E,d], W1[E,dff,d], W3[E,dff,d], W2[E,d,dff], out[T,d].
+ *    Device pointers must be 16-byte aligned (256-byte for the tensor-core
+ *    path's x_perm / h_perm / W1 / W3 / W2).
+ *  - dtype is MOE_DTYPE_BF16 (bf16 storage, fp32 accumulate) or
+ *    MOE_DTYPE_F32 (fp32 storage and arithmetic, no TF32).
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) of the device that owns the output pointer.  No entry point
+ *    synchronises the host unless it says so.
+ *  - Return value: MOE_OK (0) or a negative MOE_E* code.  Arguments are
+ *    validated on the host before anything is enqueued; a failed check
+ *    enqueues nothing.  Nothing aborts the process.
+ *  - Device-side failures (an out-of-range expert index, a bounded wait that
+ *    ran out) do not trap: the kernel records a MOE_E* code in a per-device
+ *    status word and returns.  Read it with moe_get_device_status().
+ *  - T = 0 is a valid no-op.
+ *
+ * Supported shapes: 1 <= k <= min(E, 8), 1 <= E <= 64, d % 8 == 0 (f32:
+ * d % 4 == 0).  The bf16 expert path (tcgen05 tensor cores) also needs
+ * d % 64 == 0 and dff % 64 == 0.  Anything else returns MOE_EUNSUPPORTED.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* The same type as cudaStream_t; pass a cudaStream_t (or NULL) directly. */
+typedef struct CUstream_st* moe_stream_t;
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,       /* null pointer, negative size, misaligned pointer   */
+  MOE_EUNSUPPORTED = -2, /* valid arguments outside the supported shapes      */
+  MOE_ECUDA = -3,        /* a CUDA runtime/driver call failed                 */
+  MOE_ETIMEOUT = -4,     /* a device-side bounded wait ran out (device status)*/
+  MOE_ENOMEM = -5,       /* workspace too small, or allocation failed         */
+  MOE_EDEVICE = -6       /* device-side bounds check failed (device status)   */
+};
+
+enum moe_dtype { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 };
+
+/* Short text for a status code (static storage). */
+const char* moe_status_string(int status);
+
+/* ABI version (major * 100 + minor). */
+int moe_version(void);
+
+/*
+ * Steps a1 + a2 - router (section 05, MoERouter): fp32 gate logits
+ * l[t,e] = sum_c x[t,c] Wg[e,c], then the k largest logits in descending
+ * order (equal logits: lower expert index first), then their softmax.
+ *   x[T,d], Wg[E,d]          in: dtype
+ *   topk_idx[T,k] int32      out: chosen experts, slot 0 = largest logit
+ *   topk_w[T,k]   fp32       out: gate weights, sum to 1 per token
+ *   logits_opt[T,E] fp32     out, optional (NULL to skip)
+ */
+int moe_router_topk(const void* x, const void* Wg, int T, int d, int E, int k,
+                    int32_t* topk_idx, float* topk_w, float* logits_opt,
+                    int dtype, moe_stream_t stream);
+
+/*
+ * Step a0 - RMSNorm (section 03): xn = x (mean(x^2) + eps)^-1/2 gamma,
+ * computed in fp32 and rounded once to dtype.  x[T,d], gamma[d], xn[T,d].
+ */
+int moe_rmsnorm(const void* x, const void* gamma, float eps, void* xn,
+                int T, int d, int dtype, moe_stream_t stream);
+
+/*
+ * Step a3 - dispatch (section 05, class MoE groups tokens per expert; the
+ * page notes production stacks batch tokens per expert).  With Tk = T*k and
+ * the flat pair index f = t*k + j:
+ *   counts[E]      out: n_e = #{f : topk_idx[f] == e}
+ *   offsets[E+1]   out: exclusive prefix sum of counts, offsets[E] = Tk
+ *   slot_pos[Tk]   out: row of pair f in expert-contiguous order; stable:
+ *                  within an expert, rows follow ascending f
+ *   row_src[Tk]    out: row_src[slot_pos[f]] = f / k (source token)
+ *   x_perm[Tk,d]   out: x_perm[p] = x[row_src[p]]
+ * An index outside [0,E) is skipped and sets MOE_EDEVICE in the device
+ * status; the outputs are then incomplete.
+ */
+int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
+                int32_t* counts, int32_t* offsets, int32_t* row_src, int32_t* slot_pos,
+                void* x_perm, int dtype, moe_stream_t stream);
+
+/*
+ * Step a4 - grouped gate/up GEMM with the SwiGLU fused into its epilogue
+ * (section 04): for expert e and every row p in [offsets[e], offsets[e+1]),
+ *   h_perm[p, f] = silu(sum_c x_perm[p,c] W1[e,f,c]) * sum_c x_perm[p,c] W3[e,f,c]
+ * x_perm[Tk,d] in, h_perm[Tk,dff] out, offsets[E+1] in (device).
+ * bf16: fp32 accumulation in tensor memory, h rounded once to bf16.
+ */
+int moe_expert_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3,
+                       void* h_perm, int Tk, int d, int dff, int E, int dtype, moe_stream_t stream);
+
+/*
+ * Step a5 - grouped down-projection GEMM (section 04):
+ *   y_perm[p, c] = sum_f h_perm[p,f] W2[e,c,f]   for p in expert e's rows.
+ * h_perm[Tk,dff] in, y_perm[Tk,d] out (dtype).
+ */
+int moe_expert_down(const void* h_perm, const int32_t* offsets, const void* W2,
+                    void* y_perm, int Tk, int d, int dff, int E, int dtype, moe_stream_t stream);
+
+/* Steps a4 + a5 in one call; h_perm[Tk,dff] is caller-provided scratch. */
+int moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3,
+                   const void* W2, void* h_perm, void* y_perm, int Tk, int d, int dff, int E,
+                   int dtype, moe_stream_t stream);
+
+/*
+ * Step a6 - combine fused with the un-permute (section 05, class MoE adds the
+ * chosen experts' outputs with their weights; section 06 adds the residual):
+ *   out[t,c] = sum_j topk_w[t,j] y_perm[slot_pos[t*k+j], c]  (+ residual[t,c])
+ * summed in fp32, rounded once to dtype.  residual_opt may be NULL.
+ */
+int moe_combine(const void* y_perm, const int32_t* slot_pos, const float* topk_w,
+                const void* residual_opt, void* out, int T, int d, int k, int dtype,
+                moe_stream_t stream);
+
+/* Bytes of scratch moe_forward_ws / moe_block_forward_ws need. */
+size_t moe_forward_workspace_bytes(int T, int d, int dff, int E, int k, int dtype);
+
+/*
+ * The whole layer, a1..a6, on caller-provided scratch `workspace` of at least
+ * moe_forward_workspace_bytes() bytes (256-byte aligned).  dtype selects the
+ * bf16 tensor-core path or the fp32 path.
+ */
+int moe_forward_ws(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                   void* out, int T, int d, int dff, int E, int k, int dtype,
+                   void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * The whole layer in bf16, one call.  Scratch comes from cudaMallocAsync on
+ * `stream` (the device's stream-ordered pool) and is released on the same
+ * stream.
+ */
+int moe_forward(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                void* out, int T, int d, int dff, int E, int k, moe_stream_t stream);
+
+/* As moe_forward, fp32 storage and arithmetic (CUDA-core path). */
+int moe_forward_f32(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                    void* out, int T, int d, int dff, int E, int k, moe_stream_t stream);
+
+/*
+ * Block form, a0..a6 (section 06, Block, MoE half): out = x + MoE(RMSNorm(x)).
+ * gamma[d]; the normalised activation is rounded once to dtype before the
+ * router and the experts.  _ws takes caller scratch as moe_forward_ws.
+ */
+int moe_block_forward_ws(const void* x, const void* gamma, float eps, const void* Wg,
+                         const void* W1, const void* W3, const void* W2, void* out,
+                         int T, int d, int dff, int E, int k, int dtype,
+                         void* workspace, size_t workspace_bytes, moe_stream_t stream);
+int moe_block_forward(const void* x, const void* gamma, float eps, const void* Wg,
+                      const void* W1, const void* W3, const void* W2, void* out,
+                      int T, int d, int dff, int E, int k, moe_stream_t stream);
+
+/*
+ * End-to-end call with HOST activations: copies x_host[T,d] (pinned host
+ * memory for best speed) to the device, runs moe_forward_ws, and copies the
+ * result back to out_host[T,d].  Weights stay resident on the device.
+ * `workspace` must hold moe_forward_workspace_bytes() + 2*T*d*elem bytes.
+ * Synchronises `stream` before returning, so out_host is ready on return.
+ */
+size_t moe_forward_host_workspace_bytes(int T, int d, int dff, int E, int k, int dtype);
+int moe_forward_host(const void* x_host, const void* Wg, const void* W1, const void* W3,
+                     const void* W2, void* out_host, int T, int d, int dff, int E, int k,
+                     int dtype, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Device status word of the device that owns `stream`: synchronises the
+ * stream, writes the first MOE_E* code a kernel recorded since the last reset
+ * (MOE_OK if none) to *status, and clears it when reset != 0.
+ */
+int moe_get_device_status(moe_stream_t stream, int* status, int reset);
+
+/*
+ * Limit, in nanoseconds, for every device-side spin wait launched after this
+ * call (default 2e9).  A wait that runs out records MOE_ETIMEOUT and the
+ * kernel returns early.  ns <= 0 restores the default.  Host-side setting,
+ * process-wide.
+ */
+int moe_set_wait_limit_ns(long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,417 @@
+// C-ABI entry points of libmoe (declared in include/moe.h).  Host code only:
+// argument validation, device selection, workspace layout and the order of
+// the kernels of the sparse-MoE layer ("The Evolving Transformer - 05
+// Mixtral", sections 03-06):
+//   [a0 RMSNorm] -> a1/a2 router -> a3 dispatch (rank, gather) ->
+//   a4 gate/up + SwiGLU -> a5 down -> a6 combine [+ residual].
+// Everything is enqueued on the caller's stream; no entry point reads a
+// device value on the host, so the per-expert counts never leave the GPU.
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+// First MOE_E* code any kernel recorded on this device since the last reset.
+__device__ int g_status;
+
+namespace {
+
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+
+struct DevInfo {
+  bool init;
+  int num_sms;
+  int* status;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+}  // namespace
+
+int make_ctx(const void* dev_ptr, Ctx* ctx) {
+  int dev = -1;
+  if (dev_ptr != nullptr) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, dev_ptr) == cudaSuccess &&
+        (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged)) {
+      dev = a.device;
+    } else {
+      cudaGetLastError();
+    }
+  }
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ECUDA;
+  if (dev < 0) dev = cur;
+  if (dev >= 64) return MOE_EUNSUPPORTED;
+  if (dev != cur && cudaSetDevice(dev) != cudaSuccess) return MOE_ECUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ECUDA;
+    void* sp = nullptr;
+    if (cudaGetSymbolAddress(&sp, g_status) != cudaSuccess) return MOE_ECUDA;
+    d.num_sms = sms;
+    d.status = static_cast<int*>(sp);
+    d.init = true;
+  }
+  ctx->device = dev;
+  ctx->num_sms = d.num_sms;
+  ctx->status = d.status;
+  ctx->wait_ns = g_wait_ns.load();
+  return MOE_OK;
+}
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline size_t esize(int dtype) { return dtype == MOE_DTYPE_BF16 ? 2 : 4; }
+inline int launch_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ECUDA; }
+
+#define MOE_TRY(expr)          \
+  do {                         \
+    const int rc_ = (expr);    \
+    if (rc_ != MOE_OK) return rc_; \
+  } while (0)
+
+int check_dtype(int dtype) { return (dtype == MOE_DTYPE_F32 || dtype == MOE_DTYPE_BF16) ? MOE_OK : MOE_EINVAL; }
+
+// Shape checks shared by the entry points that see tokens.
+int check_tokens(int T, int d, int E, int k, int dtype) {
+  MOE_TRY(check_dtype(dtype));
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_EINVAL;
+  if (E > 64 || k > 8) return MOE_EUNSUPPORTED;
+  if (d % (dtype == MOE_DTYPE_BF16 ? 8 : 4) != 0) return MOE_EUNSUPPORTED;
+  if (static_cast<long long>(T) * k > INT_MAX / 2) return MOE_EUNSUPPORTED;
+  return MOE_OK;
+}
+
+// Shape checks of the expert GEMMs.
+int check_ffn(int Tk, int d, int dff, int E, int dtype) {
+  MOE_TRY(check_dtype(dtype));
+  if (Tk < 0 || d <= 0 || dff <= 0 || E <= 0) return MOE_EINVAL;
+  if (E > 64) return MOE_EUNSUPPORTED;
+  if (dtype == MOE_DTYPE_BF16) {
+    if (d % 64 != 0 || dff % 64 != 0) return MOE_EUNSUPPORTED;
+    if (static_cast<long long>(E) * dff > INT_MAX / 2 || static_cast<long long>(E) * d > INT_MAX / 2)
+      return MOE_EUNSUPPORTED;
+  } else {
+    if (d % 4 != 0 || dff % 4 != 0) return MOE_EUNSUPPORTED;
+    if (Tk / 64 + E > 65535) return MOE_EUNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+int ffn_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, void* h, int Tk, int d,
+                int dff, int E, int dtype, const Ctx& c, cudaStream_t s) {
+  if (dtype == MOE_DTYPE_BF16) return launch_tc_gate_up(x_perm, offsets, W1, W3, h, Tk, d, dff, E, c, s);
+  return launch_rc(launch_ffn_f32_gate_up(static_cast<const float*>(x_perm), offsets, static_cast<const float*>(W1),
+                                          static_cast<const float*>(W3), static_cast<float*>(h), Tk, d, dff, E, c, s));
+}
+
+int ffn_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d, int dff, int E, int dtype,
+             const Ctx& c, cudaStream_t s) {
+  if (dtype == MOE_DTYPE_BF16) return launch_tc_down(h, offsets, W2, y, Tk, d, dff, E, c, s);
+  return launch_rc(launch_ffn_f32_down(static_cast<const float*>(h), offsets, static_cast<const float*>(W2),
+                                       static_cast<float*>(y), Tk, d, dff, E, c, s));
+}
+
+struct WsLayout {
+  size_t idx, w, counts, offs, row_src, slot_pos, x_perm, h, y, xn, total;
+};
+
+inline size_t al256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+WsLayout ws_layout(int T, int d, int dff, int E, int k, int dtype) {
+  const size_t es = esize(dtype);
+  const size_t Tk = static_cast<size_t>(T) * k;
+  WsLayout L;
+  size_t o = 0;
+  L.idx = o;       o = al256(o + Tk * 4);
+  L.w = o;         o = al256(o + Tk * 4);
+  L.counts = o;    o = al256(o + static_cast<size_t>(E) * 4);
+  L.offs = o;      o = al256(o + static_cast<size_t>(E + 1) * 4);
+  L.row_src = o;   o = al256(o + Tk * 4);
+  L.slot_pos = o;  o = al256(o + Tk * 4);
+  L.x_perm = o;    o = al256(o + Tk * d * es);
+  L.h = o;         o = al256(o + Tk * dff * es);
+  L.y = o;         o = al256(o + Tk * d * es);
+  L.xn = o;        o = al256(o + static_cast<size_t>(T) * d * es);
+  L.total = o;
+  return L;
+}
+
+// The layer on caller scratch; gamma != NULL selects the block form.
+int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, const void* W1, const void* W3,
+                 const void* W2, void* out, int T, int d, int dff, int E, int k, int dtype, void* ws, size_t ws_bytes,
+                 const Ctx& c, cudaStream_t s) {
+  const WsLayout L = ws_layout(T, d, dff, E, k, dtype);
+  if (ws_bytes < L.total) return MOE_ENOMEM;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  int32_t* idx = reinterpret_cast<int32_t*>(base + L.idx);
+  float* w = reinterpret_cast<float*>(base + L.w);
+  int32_t* counts = reinterpret_cast<int32_t*>(base + L.counts);
+  int32_t* offs = reinterpret_cast<int32_t*>(base + L.offs);
+  int32_t* row_src = reinterpret_cast<int32_t*>(base + L.row_src);
+  int32_t* slot_pos = reinterpret_cast<int32_t*>(base + L.slot_pos);
+  void* x_perm = base + L.x_perm;
+  void* h = base + L.h;
+  void* y = base + L.y;
+  const int Tk = T * k;
+  const void* xin = x;
+  if (gamma != nullptr) {
+    void* xn = base + L.xn;
+    MOE_TRY(launch_rc(launch_rmsnorm(x, gamma, eps, xn, T, d, dtype, c, s)));
+    xin = xn;
+  }
+  MOE_TRY(launch_rc(launch_router(xin, Wg, T, d, E, k, idx, w, nullptr, dtype, c, s)));
+  MOE_TRY(launch_rc(launch_dispatch(idx, Tk, E, k, counts, offs, row_src, slot_pos, c, s)));
+  MOE_TRY(launch_rc(launch_gather_rows(xin, row_src, x_perm, T, Tk, static_cast<size_t>(d) * esize(dtype), c, s)));
+  MOE_TRY(ffn_gate_up(x_perm, offs, W1, W3, h, Tk, d, dff, E, dtype, c, s));
+  MOE_TRY(ffn_down(h, offs, W2, y, Tk, d, dff, E, dtype, c, s));
+  MOE_TRY(launch_rc(launch_combine(y, slot_pos, w, gamma != nullptr ? x : nullptr, out, T, d, k, dtype, c, s)));
+  return MOE_OK;
+}
+
+int check_forward(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2, const void* out,
+                  int T, int d, int dff, int E, int k, int dtype) {
+  MOE_TRY(check_tokens(T, d, E, k, dtype));
+  MOE_TRY(check_ffn(T * k, d, dff, E, dtype));
+  if (T == 0) return MOE_OK;
+  const void* ptrs[] = {x, Wg, W1, W3, W2, out};
+  for (const void* p : ptrs) {
+    if (p == nullptr) return MOE_EINVAL;
+    if (!aligned(p, 16)) return MOE_EINVAL;
+  }
+  return MOE_OK;
+}
+
+int forward_alloc(const void* x, const void* gamma, float eps, const void* Wg, const void* W1, const void* W3,
+                  const void* W2, void* out, int T, int d, int dff, int E, int k, int dtype, cudaStream_t s) {
+  MOE_TRY(check_forward(x, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype));
+  if (T == 0) return MOE_OK;
+  Ctx c;
+  MOE_TRY(make_ctx(out, &c));
+  const size_t bytes = ws_layout(T, d, dff, E, k, dtype).total;
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ENOMEM;
+  }
+  const int rc = forward_impl(x, gamma, eps, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype, ws, bytes, c, s);
+  const cudaError_t fe = cudaFreeAsync(ws, s);
+  if (rc != MOE_OK) return rc;
+  return fe == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
+
+int check_eps(float eps) { return (std::isfinite(eps) && eps >= 0.0f) ? MOE_OK : MOE_EINVAL; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_EINVAL: return "invalid argument";
+    case MOE_EUNSUPPORTED: return "unsupported shape or dtype";
+    case MOE_ECUDA: return "CUDA call failed";
+    case MOE_ETIMEOUT: return "device-side wait timed out";
+    case MOE_ENOMEM: return "workspace too small or allocation failed";
+    case MOE_EDEVICE: return "device-side bounds check failed";
+    default: return "unknown status";
+  }
+}
+
+int moe_version(void) { return 100; }
+
+int moe_set_wait_limit_ns(long long ns) {
+  g_wait_ns.store(ns > 0 ? static_cast<unsigned long long>(ns) : 2000000000ull);
+  return MOE_OK;
+}
+
+int moe_router_topk(const void* x, const void* Wg, int T, int d, int E, int k, int32_t* topk_idx, float* topk_w,
+                    float* logits_opt, int dtype, moe_stream_t stream) {
+  MOE_TRY(check_tokens(T, d, E, k, dtype));
+  if (T == 0) return MOE_OK;
+  if (!x || !Wg || !topk_idx || !topk_w) return MOE_EINVAL;
+  if (!aligned(x, 16) || !aligned(Wg, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+      !aligned(logits_opt, 4))
+    return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(topk_idx, &c));
+  return launch_rc(launch_router(x, Wg, T, d, E, k, topk_idx, topk_w, logits_opt, dtype, c, stream));
+}
+
+int moe_rmsnorm(const void* x, const void* gamma, float eps, void* xn, int T, int d, int dtype, moe_stream_t stream) {
+  MOE_TRY(check_tokens(T, d, 1, 1, dtype));
+  MOE_TRY(check_eps(eps));
+  if (T == 0) return MOE_OK;
+  if (!x || !gamma || !xn || !aligned(x, 16) || !aligned(gamma, 16) || !aligned(xn, 16)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(xn, &c));
+  return launch_rc(launch_rmsnorm(x, gamma, eps, xn, T, d, dtype, c, stream));
+}
+
+int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int k, int32_t* counts,
+                int32_t* offsets, int32_t* row_src, int32_t* slot_pos, void* x_perm, int dtype,
+                moe_stream_t stream) {
+  MOE_TRY(check_tokens(T, d, E, k, dtype));
+  if (!counts || !offsets) return MOE_EINVAL;
+  if (T > 0 && (!x || !topk_idx || !row_src || !slot_pos || !x_perm)) return MOE_EINVAL;
+  if (!aligned(x, 16) || !aligned(x_perm, 16) || !aligned(topk_idx, 4) || !aligned(counts, 4) ||
+      !aligned(offsets, 4) || !aligned(row_src, 4) || !aligned(slot_pos, 4))
+    return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(offsets, &c));
+  const int Tk = T * k;
+  MOE_TRY(launch_rc(launch_dispatch(topk_idx, Tk, E, k, counts, offsets, row_src, slot_pos, c, stream)));
+  if (Tk == 0) return MOE_OK;
+  return launch_rc(launch_gather_rows(x, row_src, x_perm, T, Tk, static_cast<size_t>(d) * esize(dtype), c, stream));
+}
+
+int moe_expert_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, void* h_perm,
+                       int Tk, int d, int dff, int E, int dtype, moe_stream_t stream) {
+  MOE_TRY(check_ffn(Tk, d, dff, E, dtype));
+  if (Tk == 0) return MOE_OK;
+  const void* ptrs[] = {x_perm, offsets, W1, W3, h_perm};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(h_perm, &c));
+  return ffn_gate_up(x_perm, offsets, W1, W3, h_perm, Tk, d, dff, E, dtype, c, stream);
+}
+
+int moe_expert_down(const void* h_perm, const int32_t* offsets, const void* W2, void* y_perm, int Tk, int d, int dff,
+                    int E, int dtype, moe_stream_t stream) {
+  MOE_TRY(check_ffn(Tk, d, dff, E, dtype));
+  if (Tk == 0) return MOE_OK;
+  const void* ptrs[] = {h_perm, offsets, W2, y_perm};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(y_perm, &c));
+  return ffn_down(h_perm, offsets, W2, y_perm, Tk, d, dff, E, dtype, c, stream);
+}
+
+int moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, const void* W2,
+                   void* h_perm, void* y_perm, int Tk, int d, int dff, int E, int dtype, moe_stream_t stream) {
+  MOE_TRY(moe_expert_gate_up(x_perm, offsets, W1, W3, h_perm, Tk, d, dff, E, dtype, stream));
+  return moe_expert_down(h_perm, offsets, W2, y_perm, Tk, d, dff, E, dtype, stream);
+}
+
+int moe_combine(const void* y_perm, const int32_t* slot_pos, const float* topk_w, const void* residual_opt, void* out,
+                int T, int d, int k, int dtype, moe_stream_t stream) {
+  MOE_TRY(check_tokens(T, d, k, k, dtype));
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !slot_pos || !topk_w || !out) return MOE_EINVAL;
+  if (!aligned(y_perm, 16) || !aligned(out, 16) || !aligned(residual_opt, 16) || !aligned(slot_pos, 4) ||
+      !aligned(topk_w, 4))
+    return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(out, &c));
+  return launch_rc(launch_combine(y_perm, slot_pos, topk_w, residual_opt, out, T, d, k, dtype, c, stream));
+}
+
+size_t moe_forward_workspace_bytes(int T, int d, int dff, int E, int k, int dtype) {
+  if (check_tokens(T, d, E, k, dtype) != MOE_OK || dff <= 0) return 0;
+  return ws_layout(T, d, dff, E, k, dtype).total;
+}
+
+int moe_forward_ws(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2, void* out, int T,
+                   int d, int dff, int E, int k, int dtype, void* workspace, size_t workspace_bytes,
+                   moe_stream_t stream) {
+  MOE_TRY(check_forward(x, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype));
+  if (T == 0) return MOE_OK;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(out, &c));
+  return forward_impl(x, nullptr, 0.0f, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype, workspace, workspace_bytes, c,
+                      stream);
+}
+
+int moe_forward(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2, void* out, int T, int d,
+                int dff, int E, int k, moe_stream_t stream) {
+  return forward_alloc(x, nullptr, 0.0f, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_BF16, stream);
+}
+
+int moe_forward_f32(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2, void* out, int T,
+                    int d, int dff, int E, int k, moe_stream_t stream) {
+  return forward_alloc(x, nullptr, 0.0f, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_F32, stream);
+}
+
+int moe_block_forward_ws(const void* x, const void* gamma, float eps, const void* Wg, const void* W1, const void* W3,
+                         const void* W2, void* out, int T, int d, int dff, int E, int k, int dtype, void* workspace,
+                         size_t workspace_bytes, moe_stream_t stream) {
+  MOE_TRY(check_forward(x, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype));
+  MOE_TRY(check_eps(eps));
+  if (T == 0) return MOE_OK;
+  if (gamma == nullptr || !aligned(gamma, 16)) return MOE_EINVAL;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(out, &c));
+  return forward_impl(x, gamma, eps, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype, workspace, workspace_bytes, c,
+                      stream);
+}
+
+int moe_block_forward(const void* x, const void* gamma, float eps, const void* Wg, const void* W1, const void* W3,
+                      const void* W2, void* out, int T, int d, int dff, int E, int k, moe_stream_t stream) {
+  MOE_TRY(check_eps(eps));
+  if (T > 0 && (gamma == nullptr || !aligned(gamma, 16))) return MOE_EINVAL;
+  return forward_alloc(x, gamma, eps, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_BF16, stream);
+}
+
+size_t moe_forward_host_workspace_bytes(int T, int d, int dff, int E, int k, int dtype) {
+  const size_t base = moe_forward_workspace_bytes(T, d, dff, E, k, dtype);
+  if (base == 0) return 0;
+  const size_t act = al256(static_cast<size_t>(T) * d * esize(dtype));
+  return base + 2 * act;
+}
+
+int moe_forward_host(const void* x_host, const void* Wg, const void* W1, const void* W3, const void* W2,
+                     void* out_host, int T, int d, int dff, int E, int k, int dtype, void* workspace,
+                     size_t workspace_bytes, moe_stream_t stream) {
+  MOE_TRY(check_forward(x_host, Wg, W1, W3, W2, out_host, T, d, dff, E, k, dtype));
+  if (T == 0) return MOE_OK;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
+  const size_t need = moe_forward_host_workspace_bytes(T, d, dff, E, k, dtype);
+  if (workspace_bytes < need) return MOE_ENOMEM;
+  Ctx c;
+  MOE_TRY(make_ctx(Wg, &c));
+  const size_t base = moe_forward_workspace_bytes(T, d, dff, E, k, dtype);
+  const size_t act_bytes = static_cast<size_t>(T) * d * esize(dtype);
+  uint8_t* x_dev = static_cast<uint8_t*>(workspace) + base;
+  uint8_t* out_dev = x_dev + al256(act_bytes);
+  if (cudaMemcpyAsync(x_dev, x_host, act_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return MOE_ECUDA;
+  MOE_TRY(forward_impl(x_dev, nullptr, 0.0f, Wg, W1, W3, W2, out_dev, T, d, dff, E, k, dtype, workspace, base, c,
+                       stream));
+  if (cudaMemcpyAsync(out_host, out_dev, act_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MOE_ECUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
+
+int moe_get_device_status(moe_stream_t stream, int* status, int reset) {
+  if (status == nullptr) return MOE_EINVAL;
+  int dev = 0;
+  if (cudaStreamGetDevice(stream, &dev) != cudaSuccess) return MOE_ECUDA;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ECUDA;
+  if (dev != cur && cudaSetDevice(dev) != cudaSuccess) return MOE_ECUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ECUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return MOE_ECUDA;
+  if (reset) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_status, &z, sizeof(int)) != cudaSuccess) return MOE_ECUDA;
+  }
+  *status = v;
+  return MOE_OK;
+}
+
+}  // extern "C"

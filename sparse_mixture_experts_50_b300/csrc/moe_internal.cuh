@@ -1,0 +1,56 @@
+// Internal declarations shared by the libmoe translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Per-call context: the device that owns the output, its SM count, the
+// address of that device's status word and the spin-wait limit.
+struct Ctx {
+  int device;
+  int num_sms;
+  int* status;                 // device address of the per-device status word
+  unsigned long long wait_ns;  // bounded-wait limit for spinning kernels
+};
+
+// Sets the calling thread's current device to the one owning `dev_ptr`
+// (or keeps the current device if the pointer is not a device pointer) and
+// fills `ctx`.  Returns MOE_OK or MOE_ECUDA.
+int make_ctx(const void* dev_ptr, Ctx* ctx);
+
+// Records `code` in the device status word unless one is already recorded.
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ---- launchers (each returns a cudaError_t from the launch) --------------
+cudaError_t launch_router(const void* x, const void* Wg, int T, int d, int E, int k,
+                          int32_t* idx, float* w, float* logits, int dtype,
+                          const Ctx& c, cudaStream_t s);
+cudaError_t launch_rmsnorm(const void* x, const void* gamma, float eps, void* xn, int T, int d,
+                           int dtype, const Ctx& c, cudaStream_t s);
+cudaError_t launch_dispatch(const int32_t* idx, int Tk, int E, int k, int32_t* counts,
+                            int32_t* offsets, int32_t* row_src, int32_t* slot_pos,
+                            const Ctx& c, cudaStream_t s);
+cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, void* x_perm, int T, int Tk,
+                               size_t row_bytes, const Ctx& c, cudaStream_t s);
+cudaError_t launch_combine(const void* y, const int32_t* slot_pos, const float* w,
+                           const void* residual, void* out, int T, int d, int k, int dtype,
+                           const Ctx& c, cudaStream_t s);
+cudaError_t launch_ffn_f32_gate_up(const float* x_perm, const int32_t* offsets, const float* W1,
+                                   const float* W3, float* h, int Tk, int d, int dff, int E,
+                                   const Ctx& c, cudaStream_t s);
+cudaError_t launch_ffn_f32_down(const float* h, const int32_t* offsets, const float* W2, float* y,
+                                int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
+// bf16 tcgen05 path; returns MOE_* status (tensor-map encoding can fail).
+int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3,
+                      void* h, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
+int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d,
+                   int dff, int E, const Ctx& c, cudaStream_t s);
+
+}  // namespace moe

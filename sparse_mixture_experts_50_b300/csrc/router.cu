@@ -1,0 +1,189 @@
+// Steps a0-a2 of the sparse-MoE layer: RMSNorm prologue (block form) and the
+// router ("The Evolving Transformer - 05 Mixtral", section 03 RMSNorm and
+// section 05 MoERouter).
+//
+// Router: one warp per token.  Each lane accumulates fp32 partial dot products
+// of its 16-byte slices of x[t] with every gate row, a butterfly all-reduce
+// gives every lane all E logits, and every lane then runs the same top-k
+// (descending, equal logits keep the lower index) and the softmax over the k
+// chosen logits.  The page's order - softmax over all E, top-k, renormalise -
+// gives the same weights because the normaliser over all E cancels.
+#include <math.h>
+
+#include "moe_internal.cuh"
+#include "vec.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int EMAX, typename TIn>
+__global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __restrict__ x, const TIn* __restrict__ Wg,
+                                                               int T, int d, int E, int k, int32_t* __restrict__ idx,
+                                                               float* __restrict__ w, float* __restrict__ logits) {
+  constexpr int V = VecOf<TIn>::n;
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = gwarp; t < T; t += nwarps) {
+    float acc[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) acc[e] = 0.0f;
+    const TIn* xr = x + static_cast<size_t>(t) * d;
+    for (int c = lane * V; c < d; c += 32 * V) {
+      float xv[V];
+      load_vec(xr + c, xv);
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) {
+        if (e < E) {
+          float gv[V];
+          load_vec(Wg + static_cast<size_t>(e) * d + c, gv);
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], gv[i], acc[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      if (e < E) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[e] += __shfl_xor_sync(0xFFFFFFFFu, acc[e], o);
+      }
+    }
+    // Top-k, identical in every lane.  Strict '>' over ascending e keeps the
+    // lower index on equal logits; a NaN never wins but a slot is always filled.
+    uint64_t taken = 0;
+    float sel_l[8];
+    int sel_i[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sel_l[j] = 0.0f;
+      sel_i[j] = 0;
+      if (j < k) {
+        float best = 0.0f;
+        int bi = -1;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+          if (e < E && !((taken >> e) & 1ull) && (bi < 0 || acc[e] > best)) {
+            best = acc[e];
+            bi = e;
+          }
+        }
+        taken |= 1ull << bi;
+        sel_l[j] = best;
+        sel_i[j] = bi;
+      }
+    }
+    // Softmax over the k chosen logits, shifted by the largest.
+    float ex[8];
+    float sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      ex[j] = (j < k) ? expf(sel_l[j] - sel_l[0]) : 0.0f;
+      sum += ex[j];
+    }
+    if (lane < k) {
+      float my_e = 0.0f;
+      int my_i = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j == lane) {
+          my_e = ex[j];
+          my_i = sel_i[j];
+        }
+      }
+      idx[static_cast<size_t>(t) * k + lane] = my_i;
+      w[static_cast<size_t>(t) * k + lane] = my_e / sum;
+    }
+    if (logits != nullptr) {
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) {
+        if (e < E && (e & 31) == lane) logits[static_cast<size_t>(t) * E + e] = acc[e];
+      }
+    }
+  }
+}
+
+// RMSNorm, one warp per row: fp32 mean of squares, xn = x * r * gamma with
+// r = 1 / sqrt(mean + eps), rounded once to the storage type.
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TIn* __restrict__ x, const TIn* __restrict__ gamma,
+                                                           float eps, TIn* __restrict__ xn, int T, int d) {
+  constexpr int V = VecOf<TIn>::n;
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = gwarp; t < T; t += nwarps) {
+    const TIn* xr = x + static_cast<size_t>(t) * d;
+    float ss = 0.0f;
+    for (int c = lane * V; c < d; c += 32 * V) {
+      float v[V];
+      load_vec(xr + c, v);
+#pragma unroll
+      for (int i = 0; i < V; ++i) ss = fmaf(v[i], v[i], ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    const float r = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+    TIn* outr = xn + static_cast<size_t>(t) * d;
+    for (int c = lane * V; c < d; c += 32 * V) {
+      float v[V], g[V];
+      load_vec(xr + c, v);
+      load_vec(gamma + c, g);
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[i] = (v[i] * r) * g[i];
+      store_vec(outr + c, v);
+    }
+  }
+}
+
+int grid_for(int warps_needed, const Ctx& c) {
+  const int per_block = kThreads / 32;
+  int blocks = (warps_needed + per_block - 1) / per_block;
+  const int cap = c.num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  return blocks < 1 ? 1 : blocks;
+}
+
+template <typename TIn>
+cudaError_t launch_router_t(const void* x, const void* Wg, int T, int d, int E, int k, int32_t* idx, float* w,
+                            float* logits, const Ctx& c, cudaStream_t s) {
+  const int grid = grid_for(T, c);
+  const TIn* xp = static_cast<const TIn*>(x);
+  const TIn* gp = static_cast<const TIn*>(Wg);
+  if (E <= 8) {
+    router_topk_kernel<8, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits);
+  } else if (E <= 16) {
+    router_topk_kernel<16, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits);
+  } else if (E <= 32) {
+    router_topk_kernel<32, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits);
+  } else {
+    router_topk_kernel<64, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router(const void* x, const void* Wg, int T, int d, int E, int k, int32_t* idx, float* w,
+                          float* logits, int dtype, const Ctx& c, cudaStream_t s) {
+  if (dtype == MOE_DTYPE_BF16) return launch_router_t<__nv_bfloat16>(x, Wg, T, d, E, k, idx, w, logits, c, s);
+  return launch_router_t<float>(x, Wg, T, d, E, k, idx, w, logits, c, s);
+}
+
+cudaError_t launch_rmsnorm(const void* x, const void* gamma, float eps, void* xn, int T, int d, int dtype,
+                           const Ctx& c, cudaStream_t s) {
+  const int grid = grid_for(T, c);
+  if (dtype == MOE_DTYPE_BF16) {
+    rmsnorm_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+                                                            static_cast<const __nv_bfloat16*>(gamma), eps,
+                                                            static_cast<__nv_bfloat16*>(xn), T, d);
+  } else {
+    rmsnorm_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), static_cast<const float*>(gamma),
+                                                    eps, static_cast<float*>(xn), T, d);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe
