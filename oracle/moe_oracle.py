@@ -26,7 +26,9 @@ Readings where the pages are silent:
   * Equal router probabilities keep the lower expert index first.
   * In the block form the normalised activation is rounded once to bf16
     (round to nearest even) before the router and the experts, as a bf16
-    layer stores it; everything else stays in fp64.
+    layer stores it.  That rounding is a quantisation decision, so it is
+    taken from an fp32 value, the precision the block workload fixes for
+    its norm ("fp32 norm"); everything else stays in fp64.
 
 Parity pins for every function here live in tests/test_oracle_pins.py.
 """
@@ -67,6 +69,16 @@ def rmsnorm(x, gamma, eps) -> np.ndarray:
     g = f64(gamma)
     ms = np.mean(x * x, axis=-1, keepdims=True)
     return x / np.sqrt(ms + eps) * g
+
+
+def rmsnorm_fp32(x, gamma, eps) -> np.ndarray:
+    """Section 03 (RMSNorm) in fp32 arithmetic: mean of squares, then
+    (x * (mean + eps)^-1/2) * gamma, every operation rounded to fp32."""
+    x32 = f64(x).astype(np.float32)
+    g32 = f64(gamma).astype(np.float32)
+    ms = np.mean(x32 * x32, axis=-1, keepdims=True, dtype=np.float32)
+    r = np.float32(1.0) / np.sqrt(ms + np.float32(eps))
+    return (x32 * r) * g32
 
 
 # ---------------------------------------------------------------- router
@@ -171,8 +183,9 @@ def moe_forward(x, Wg, W1, W3, W2, k):
 
 
 def block_normed_input(x, gamma, eps) -> np.ndarray:
-    """Section 06 (Block), MoE half: the bf16-rounded RMSNorm(x) fed to the MoE."""
-    return round_to_bf16(rmsnorm(x, gamma, eps))
+    """Section 06 (Block), MoE half: the bf16-rounded RMSNorm(x) fed to the MoE
+    (the fp32 norm, rounded once)."""
+    return round_to_bf16(rmsnorm_fp32(x, gamma, eps).astype(np.float64))
 
 
 def block_forward(x, gamma, eps, Wg, W1, W3, W2, k):

@@ -320,6 +320,20 @@ def pin_rmsnorm_mpmath(o):
             assert abs(got[t, c] - float(mpmath.mpf(float(x[t, c])) * inv * mpmath.mpf(float(g[c])))) < 1e-15
 
 
+def pin_rmsnorm_fp32_within_rounding(o):
+    """The fp32 norm agrees with the exact (fp64) one: after the bf16 rounding
+    the two differ by at most one bf16 step, in a tiny fraction of elements."""
+    r = _rng(63)
+    x = torch.from_numpy(r.standard_normal((64, 512))).to(torch.bfloat16)
+    g = torch.from_numpy(1.0 + 0.02 * r.standard_normal(512)).to(torch.bfloat16)
+    exact = o.rmsnorm(x, g, 1e-5)
+    f32 = o.rmsnorm_fp32(x, g, 1e-5).astype(np.float64)
+    assert np.max(np.abs(f32 - exact) / np.abs(exact)) < 2e-6  # a few fp32 rounding steps
+    a, b = o.round_to_bf16(exact), o.block_normed_input(x, g, 1e-5)
+    step = np.ldexp(1.0, np.frexp(np.abs(a))[1] - 8)
+    assert np.all(np.abs(a - b) <= step) and np.mean(a != b) < 1e-3
+
+
 def pin_round_to_bf16(o):
     """fp64 -> bf16 rounding: hand ties, and torch's fp32 -> bf16 on fp32 inputs."""
     one = 1.0

@@ -147,6 +147,11 @@ def _hidden_no_gate(m):
     m.swiglu_hidden = lambda x, W1e, W3e: m.f64(x) @ m.f64(W3e).T
 
 
+def _rms32_no_square(m):
+    m.rmsnorm_fp32 = lambda x, g, eps: (m.f64(x) / np.sqrt(np.abs(np.mean(m.f64(x), -1, keepdims=True)) + eps)
+                                        * m.f64(g)).astype(np.float32)
+
+
 def _two_matrix_expert(m):
     m.expert_param_shapes = lambda d, F: [(F, d), (d, F)]
 
@@ -156,7 +161,7 @@ MUTANTS = {f.__name__[1:]: f for f in [
     _ties_to_higher_index, _drop_gate_weight, _only_first_slot, _transposed_down,
     _gate_transposed, _rms_no_square, _rms_no_eps, _rms_no_gamma, _bf16_truncates,
     _block_no_residual, _block_unnormalised, _two_matrix_expert, _dispatch_unstable,
-    _dispatch_token_not_pair, _hidden_no_gate]}
+    _dispatch_token_not_pair, _hidden_no_gate, _rms32_no_square]}
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
