@@ -1,0 +1,48 @@
+"""Bounded device waits (GPU): a wait that runs out is reported, not hung.
+
+The expert GEMM kernel bounds every spin on an mbarrier by a time limit set
+with moe_set_wait_limit_ns.  With a 1 ns limit the first wait that has to
+spin gives up: the kernel records MOE_ETIMEOUT, drains the copies and MMAs it
+already issued (those drains keep a 2 s floor), frees its tensor memory and
+returns.  The test checks the status and that the same context then computes
+correct results with the default limit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.moe_oracle as O
+from parity import check_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from sparse_mixture_experts_50_b300 import binding as B
+    r = np.random.default_rng(2)
+    E, d, F = 8, 512, 1024
+    counts = [300, 0, 129, 64, 1, 500, 7, 255]
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    Tk = int(offsets[-1])
+    x = torch.from_numpy(r.standard_normal((Tk, d))).to(torch.bfloat16).cuda()
+    W1, W3 = (torch.from_numpy(r.standard_normal((E, F, d)) * 0.05).to(torch.bfloat16).cuda() for _ in range(2))
+    off = torch.from_numpy(offsets).int().cuda()
+    B.moe_get_device_status(reset=True)
+    try:
+        B.moe_set_wait_limit_ns(1)
+        B.moe_expert_gate_up(x, off, W1, W3)
+        status = B.moe_get_device_status(reset=True)
+    finally:
+        B.moe_set_wait_limit_ns(0)  # back to the default limit
+    assert status == B.MOE_ETIMEOUT
+    h = B.moe_expert_gate_up(x, off, W1, W3)
+    assert B.moe_get_device_status(reset=True) == 0
+    xc, W1c, W3c = x.cpu(), W1.cpu(), W3.cpu()
+    ref = np.zeros((Tk, F))
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            ref[a:b] = O.swiglu_hidden(xc[a:b], W1c[e], W3c[e])
+    check_close(to_np(h), ref, "bf16", "h after a timed-out launch")
