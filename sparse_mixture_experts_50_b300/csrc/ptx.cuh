@@ -56,13 +56,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
+  // try_wait already suspends for a while before reporting "not yet", so the
+  // clock and the abort flag are checked after every failed attempt.
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (abort_flag != nullptr && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return false;
 }
