@@ -189,6 +189,34 @@ int moe_forward_host(const void* x_host, const void* Wg, const void* W1, const v
                      int dtype, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * Scratch size built into moe_forward_noalloc (16 MiB per GPU).
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * The whole bf16 layer, as moe_forward, for callers that must not allocate
+ * device memory while they run: for example an application whose memory
+ * manager owns the device budget and forbids allocation after start-up, or a
+ * latency-critical loop where an allocation could synchronise the device.
+ * The pages have no counterpart; this is a deployment variant of moe_forward.
+ *  - Scratch is a 16 MiB (MOE_NOALLOC_SCRATCH_BYTES) array inside the
+ *    library's device image: every GPU that loads the library holds it until
+ *    the process exits.  Nothing is allocated per call (no cudaMalloc,
+ *    cudaMallocAsync or cudaFree).
+ *  - A layer that needs more scratch than that, i.e.
+ *    moe_forward_workspace_bytes(T, d, dff, E, k, MOE_DTYPE_BF16) >
+ *    MOE_NOALLOC_SCRATCH_BYTES (at d=4096, d_ff=14336, k=2: T > 170), is
+ *    rejected with MOE_ENOMEM before anything is enqueued.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls share the one array, and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero, but calls that overlap on the GPU
+ *    (other streams, other host threads) race on it: serialise them.
+ */
+int moe_forward_noalloc(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                        void* out, int T, int d, int dff, int E, int k, moe_stream_t stream);
+
+/*
  * Device status word of the device that owns `stream`: synchronises the
  * stream, writes the first MOE_E* code a kernel recorded since the last reset
  * (MOE_OK if none) to *status, and clears it when reset != 0.

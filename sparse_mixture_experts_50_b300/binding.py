@@ -47,6 +47,7 @@ SIGNATURES = {
     "moe_block_forward": (_I, [_P, _P, _F, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_forward_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "moe_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_get_device_status": (_I, [_P, ctypes.POINTER(_I), _I]),
     "moe_set_wait_limit_ns": (_I, [_LL]),
 }
@@ -294,6 +295,19 @@ def moe_forward_host(x_host, Wg, W1, W3, W2, k, ws, out_host=None, stream=None):
                                                       dff, E, k, _dtype(x_host), _p(ws), ws.numel(),
                                                       _stream(stream)))
     return out_host
+
+
+def moe_forward_noalloc(x, Wg, W1, W3, W2, k, out=None, stream=None):
+    """The bf16 layer with the library's built-in scratch (no device
+    allocation by the library; see include/moe.h for its limit)."""
+    _dev(x, Wg, W1, W3, W2, out)
+    T, d = x.shape
+    E, dff, _ = W1.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check("moe_forward_noalloc", lib().moe_forward_noalloc(_p(x), _p(Wg), _p(W1), _p(W3), _p(W2), _p(out), T, d,
+                                                            dff, E, k, _stream(stream)))
+    return out
 
 
 def moe_get_device_status(reset: bool = True, stream=None) -> int:

@@ -415,3 +415,55 @@ int moe_get_device_status(moe_stream_t stream, int* status, int reset) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_forward_noalloc: the bf16 layer for callers that must not allocate
+// device memory while they run (for example an application whose memory
+// manager owns the whole device budget and forbids allocation after start-up,
+// or a latency-critical loop where a cudaMalloc could synchronise the device).
+// Its scratch is this file-scope array: it is part of the library's device
+// image, so every GPU that loads the library holds it until the process
+// exits, and all calls share it.
+namespace moe {
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current (in host code the symbol's name is only a host-side handle).
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+int noalloc_scratch(int device, void** ptr) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[device] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ECUDA;
+    }
+    g_noalloc_ptr[device] = p;
+  }
+  *ptr = g_noalloc_ptr[device];
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_forward_noalloc(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                                   void* out, int T, int d, int dff, int E, int k, moe_stream_t stream) {
+  MOE_TRY(check_forward(x, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_BF16));
+  if (T == 0) return MOE_OK;
+  const size_t need = ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16).total;
+  if (need > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ENOMEM;
+  Ctx c;
+  MOE_TRY(make_ctx(out, &c));
+  void* scratch = nullptr;
+  MOE_TRY(noalloc_scratch(c.device, &scratch));
+  // Every step writes all the scratch it later reads (indices, weights,
+  // permuted rows, h, y), so nothing left by an earlier call is used and
+  // nothing needs clearing.
+  return forward_impl(x, nullptr, 0.0f, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_BF16, scratch,
+                      MOE_NOALLOC_SCRATCH_BYTES, c, stream);
+}
