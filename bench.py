@@ -352,6 +352,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workloads", default=",".join(ALL_BENCH))
+    ap.add_argument("--headline", default=HEADLINE, choices=ALL_BENCH,
+                    help="workload of the JSON line's value (default: Mixtral-shape decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -360,9 +362,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    head_name = args.headline
     names = [n for n in args.workloads.split(",") if n]
-    if HEADLINE not in names:
-        names.insert(0, HEADLINE)
+    if head_name not in names:
+        names.insert(0, head_name)
 
     if args.impl == "reference":
         if rank != 0:
@@ -372,12 +375,12 @@ def main():
         for _ in range(args.warmup):
             pass  # the oracle has no warm-up state; each step is a fresh evaluation
         for _ in range(max(1, min(args.steps, 3))):
-            samples.append(oracle_sample(HEADLINE))
+            samples.append(oracle_sample(head_name))
         v = statistics.median(s["value"] for s in samples)
         line = {"metric": METRIC, "value": v, "unit": "tokens/s", "impl": "reference", "n_gpus": 1,
-                "steps": len(samples), "warmup": args.warmup, "ms_per_step": 1e3 * mw.get(HEADLINE).T / v,
+                "steps": len(samples), "warmup": args.warmup, "ms_per_step": 1e3 * mw.get(head_name).T / v,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config_of(HEADLINE, 1),
+                "data": "synthetic", "config": config_of(head_name, 1),
                 "cpu_baseline": {**samples[0], "value": v},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "wall_s": time.perf_counter() - t0}
@@ -398,10 +401,10 @@ def main():
     results = {}
     head_layer = None
     for name in names:
-        if name == HEADLINE:
+        if name == head_name:
             clocks.start()
         res, layer = bench_workload(name, shared, args, device, peaks, dist_on)
-        if name == HEADLINE:
+        if name == head_name:
             res["clocks"] = clocks.stop()
             head_layer = layer
         else:
@@ -409,7 +412,7 @@ def main():
         results[name] = res
         torch.cuda.empty_cache()
 
-    head = results[HEADLINE]
+    head = results[head_name]
     # Whole job: tokens of all ranks over the slowest rank's timed region.
     t_local = head["ms_per_step"] * args.steps * 1e-3
     t_max = t_local
@@ -417,7 +420,7 @@ def main():
         tt = torch.tensor([t_local], device=device)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         t_max = float(tt.item())
-    value = world * mw.get(HEADLINE).T * args.steps / t_max
+    value = world * mw.get(head_name).T * args.steps / t_max
 
     e2e = None if args.no_e2e else e2e_leg(head_layer, args.steps, args.warmup)
     if dist_on and e2e is not None:
@@ -426,17 +429,17 @@ def main():
         e2e["value"] = float(tt.item()) * world
 
     if rank == 0:
-        cpu = None if (args.no_cpu_baseline or dist_on) else oracle_sample(HEADLINE)
+        cpu = None if (args.no_cpu_baseline or dist_on) else oracle_sample(head_name)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_of(HEADLINE, world), "impl": "native",
+            "config": config_of(head_name, world), "impl": "native",
             "roofline": {k: head["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
             "roofline_detail": {**head["roofline"], "peak_source": peaks["source"],
                                 "layer_frac": head["layer_roofline_frac"]},
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": KERNELS_PER_STEP[mw.get(HEADLINE).block] * args.steps,
+            "gpu_launches": KERNELS_PER_STEP[mw.get(head_name).block] * args.steps,
             "clocks": head.get("clocks"),
             "workloads": {n: {k: v for k, v in r.items() if k not in ("clocks",)} for n, r in results.items()},
         }

@@ -11,8 +11,8 @@
 // in shared memory give the offset of each warp.  So the rows of an expert
 // follow ascending f: ascending token, then slot.
 //
-// gather kernel (many CTAs): x_perm[p] = x[row_src[p]], one warp per row,
-// 16-byte loads and stores.
+// gather kernel (many CTAs): x_perm[p] = x[row_src[p]], a flat grid-stride
+// loop over 16-byte chunks of the permuted rows.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -95,26 +95,17 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const uint4
                                                                      const int32_t* __restrict__ row_src,
                                                                      uint4* __restrict__ x_perm, int Tk, int T,
                                                                      int vecs_per_row, int* status) {
-  const int lane = threadIdx.x & 31;
-  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (int p = gwarp; p < Tk; p += nwarps) {
-    const int t = row_src[p];
+  const long long total = static_cast<long long>(Tk) * vecs_per_row;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int p = static_cast<int>(i / vecs_per_row);
+    const int v = static_cast<int>(i - static_cast<long long>(p) * vecs_per_row);
+    const int t = __ldg(row_src + p);
     if (t < 0 || t >= T) {
-      if (lane == 0) record_status(status, MOE_EDEVICE);
+      if (v == 0) record_status(status, MOE_EDEVICE);
       continue;
     }
-    const uint4* src = x + static_cast<size_t>(t) * vecs_per_row;
-    uint4* dst = x_perm + static_cast<size_t>(p) * vecs_per_row;
-    int v = lane;
-    for (; v + 96 < vecs_per_row; v += 128) {
-      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), d = __ldg(src + v + 96);
-      dst[v] = a;
-      dst[v + 32] = b;
-      dst[v + 64] = c;
-      dst[v + 96] = d;
-    }
-    for (; v < vecs_per_row; v += 32) dst[v] = __ldg(src + v);
+    x_perm[i] = __ldg(x + static_cast<size_t>(t) * vecs_per_row + v);
   }
 }
 
@@ -133,12 +124,11 @@ cudaError_t launch_dispatch(const int32_t* idx, int Tk, int E, int k, int32_t* c
 cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, void* x_perm, int T, int Tk,
                                size_t row_bytes, const Ctx& c, cudaStream_t s) {
   const int vecs = static_cast<int>(row_bytes / 16);
-  const int per_block = kGatherThreads / 32;
-  int blocks = (Tk + per_block - 1) / per_block;
+  long long blocks = (static_cast<long long>(Tk) * vecs + kGatherThreads - 1) / kGatherThreads;
   const int cap = c.num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  gather_rows_kernel<<<blocks, kGatherThreads, 0, s>>>(static_cast<const uint4*>(x), row_src,
+  gather_rows_kernel<<<static_cast<int>(blocks), kGatherThreads, 0, s>>>(static_cast<const uint4*>(x), row_src,
                                                        static_cast<uint4*>(x_perm), Tk, T, vecs, c.status);
   return cudaGetLastError();
 }

@@ -2,11 +2,14 @@
 // router ("The Evolving Transformer - 05 Mixtral", section 03 RMSNorm and
 // section 05 MoERouter).
 //
-// Router: one warp per token.  Each lane accumulates fp32 partial dot products
-// of its 16-byte slices of x[t] with every gate row, a butterfly all-reduce
-// gives every lane all E logits, and every lane then runs the same top-k
+// Router: a group of 32-256 threads per token (one warp for large batches,
+// up to a whole CTA for small ones).  Each thread accumulates fp32 partial dot
+// products of its 16-byte slices of x[t] with every gate row; a butterfly
+// all-reduce inside each warp and a fixed-order sum over the group's warps
+// give every thread all E logits, and every thread then runs the same top-k
 // (descending, equal logits keep the lower index) and the softmax over the k
-// chosen logits.  The page's order - softmax over all E, top-k, renormalise -
+// chosen logits.  The summation order depends on the group size, so logits
+// can differ in the last fp32 bit between batch sizes.  The page's order - softmax over all E, top-k, renormalise -
 // gives the same weights because the normaliser over all E cancels.
 #include <math.h>
 
@@ -18,29 +21,39 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int EMAX, typename TIn>
+// TPT threads cooperate on one token (a warp, or several warps of the CTA
+// when the batch is too small to fill the GPU with one warp per token).
+template <int EMAX, int TPT, typename TIn>
 __global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __restrict__ x, const TIn* __restrict__ Wg,
                                                                int T, int d, int E, int k, int32_t* __restrict__ idx,
                                                                float* __restrict__ w, float* __restrict__ logits) {
   constexpr int V = VecOf<TIn>::n;
+  constexpr int WPT = TPT / 32;              // warps per token
+  constexpr int TOK_PER_BLOCK = kThreads / TPT;
+  __shared__ float part[WPT > 1 ? kThreads / 32 : 1][EMAX];
   const int lane = threadIdx.x & 31;
-  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (int t = gwarp; t < T; t += nwarps) {
+  const int warp = threadIdx.x >> 5;
+  const int slot = threadIdx.x / TPT;        // token of this thread within the block
+  const int tt = threadIdx.x % TPT;          // thread within the token
+  for (int base = blockIdx.x * TOK_PER_BLOCK; base < T; base += gridDim.x * TOK_PER_BLOCK) {
+    const int t = base + slot;
+    const bool valid = t < T;                // uniform across each warp (TPT >= 32)
     float acc[EMAX];
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) acc[e] = 0.0f;
-    const TIn* xr = x + static_cast<size_t>(t) * d;
-    for (int c = lane * V; c < d; c += 32 * V) {
-      float xv[V];
-      load_vec(xr + c, xv);
+    if (valid) {
+      const TIn* xr = x + static_cast<size_t>(t) * d;
+      for (int c = tt * V; c < d; c += TPT * V) {
+        float xv[V];
+        load_vec(xr + c, xv);
 #pragma unroll
-      for (int e = 0; e < EMAX; ++e) {
-        if (e < E) {
-          float gv[V];
-          load_vec(Wg + static_cast<size_t>(e) * d + c, gv);
+        for (int e = 0; e < EMAX; ++e) {
+          if (e < E) {
+            float gv[V];
+            load_vec(Wg + static_cast<size_t>(e) * d + c, gv);
 #pragma unroll
-          for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], gv[i], acc[e]);
+            for (int i = 0; i < V; ++i) acc[e] = fmaf(xv[i], gv[i], acc[e]);
+          }
         }
       }
     }
@@ -51,8 +64,26 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __rest
         for (int o = 16; o > 0; o >>= 1) acc[e] += __shfl_xor_sync(0xFFFFFFFFu, acc[e], o);
       }
     }
-    // Top-k, identical in every lane.  Strict '>' over ascending e keeps the
-    // lower index on equal logits; a NaN never wins but a slot is always filled.
+    if (WPT > 1) {
+      if (lane == 0) {
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) part[warp][e] = acc[e];
+      }
+      __syncthreads();
+      const int w0 = slot * WPT;
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) {
+        float s = part[w0][e];
+#pragma unroll
+        for (int q = 1; q < WPT; ++q) s += part[w0 + q][e];
+        acc[e] = s;
+      }
+      __syncthreads();
+    }
+    if (!valid) continue;
+    // Top-k, identical in every thread of the token.  Strict '>' over
+    // ascending e keeps the lower index on equal logits; a NaN never wins
+    // but a slot is always filled.
     uint64_t taken = 0;
     float sel_l[8];
     int sel_i[8];
@@ -83,23 +114,23 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __rest
       ex[j] = (j < k) ? expf(sel_l[j] - sel_l[0]) : 0.0f;
       sum += ex[j];
     }
-    if (lane < k) {
+    if (tt < k) {
       float my_e = 0.0f;
       int my_i = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (j == lane) {
+        if (j == tt) {
           my_e = ex[j];
           my_i = sel_i[j];
         }
       }
-      idx[static_cast<size_t>(t) * k + lane] = my_i;
-      w[static_cast<size_t>(t) * k + lane] = my_e / sum;
+      idx[static_cast<size_t>(t) * k + tt] = my_i;
+      w[static_cast<size_t>(t) * k + tt] = my_e / sum;
     }
     if (logits != nullptr) {
 #pragma unroll
       for (int e = 0; e < EMAX; ++e) {
-        if (e < E && (e & 31) == lane) logits[static_cast<size_t>(t) * E + e] = acc[e];
+        if (e < E && e == tt) logits[static_cast<size_t>(t) * E + e] = acc[e];
       }
     }
   }
@@ -146,20 +177,45 @@ int grid_for(int warps_needed, const Ctx& c) {
   return blocks < 1 ? 1 : blocks;
 }
 
+// Threads per token: one warp when the batch fills the GPU with warps,
+// up to a whole CTA for small batches (decode), so that every token's dot
+// products are spread over enough threads to keep loads in flight.
+int threads_per_token(int T, const Ctx& c) {
+  int tpt = 32;
+  while (tpt < kThreads && static_cast<long long>(T) * tpt < static_cast<long long>(c.num_sms) * 2048) tpt *= 2;
+  return tpt;
+}
+
+template <int EMAX, typename TIn>
+void launch_router_e(const TIn* xp, const TIn* gp, int T, int d, int E, int k, int32_t* idx, float* w, float* logits,
+                     const Ctx& c, cudaStream_t s) {
+  const int tpt = threads_per_token(T, c);
+  const int per_block = kThreads / tpt;
+  int grid = (T + per_block - 1) / per_block;
+  const int cap = c.num_sms * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  switch (tpt) {
+    case 32: router_topk_kernel<EMAX, 32, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits); break;
+    case 64: router_topk_kernel<EMAX, 64, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits); break;
+    case 128: router_topk_kernel<EMAX, 128, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits); break;
+    default: router_topk_kernel<EMAX, 256, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits); break;
+  }
+}
+
 template <typename TIn>
 cudaError_t launch_router_t(const void* x, const void* Wg, int T, int d, int E, int k, int32_t* idx, float* w,
                             float* logits, const Ctx& c, cudaStream_t s) {
-  const int grid = grid_for(T, c);
   const TIn* xp = static_cast<const TIn*>(x);
   const TIn* gp = static_cast<const TIn*>(Wg);
   if (E <= 8) {
-    router_topk_kernel<8, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits);
+    launch_router_e<8, TIn>(xp, gp, T, d, E, k, idx, w, logits, c, s);
   } else if (E <= 16) {
-    router_topk_kernel<16, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits);
+    launch_router_e<16, TIn>(xp, gp, T, d, E, k, idx, w, logits, c, s);
   } else if (E <= 32) {
-    router_topk_kernel<32, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits);
+    launch_router_e<32, TIn>(xp, gp, T, d, E, k, idx, w, logits, c, s);
   } else {
-    router_topk_kernel<64, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits);
+    launch_router_e<64, TIn>(xp, gp, T, d, E, k, idx, w, logits, c, s);
   }
   return cudaGetLastError();
 }
