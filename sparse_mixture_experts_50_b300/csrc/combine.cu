@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const TIo* __restrict
                                                            const float* __restrict__ w,
                                                            const TIo* __restrict__ residual, TIo* __restrict__ out,
                                                            int T, int d, int k, int* status) {
+  pdl_enter();
   constexpr int V = VecOf<TIo>::n;
   const int vecs = d / V;
   const long long total = static_cast<long long>(T) * vecs;
@@ -68,11 +69,11 @@ cudaError_t launch_combine(const void* y, const int32_t* slot_pos, const float* 
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (dtype == MOE_DTYPE_BF16) {
-    combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), kThreads, 0, s>>>(
+    launch_pdl(combine_kernel<__nv_bfloat16>, static_cast<int>(blocks), kThreads, 0, s, 
         static_cast<const __nv_bfloat16*>(y), slot_pos, w, static_cast<const __nv_bfloat16*>(residual),
         static_cast<__nv_bfloat16*>(out), T, d, k, c.status);
   } else {
-    combine_kernel<float><<<static_cast<int>(blocks), kThreads, 0, s>>>(static_cast<const float*>(y), slot_pos, w,
+    launch_pdl(combine_kernel<float>, static_cast<int>(blocks), kThreads, 0, s, static_cast<const float*>(y), slot_pos, w,
                                                       static_cast<const float*>(residual), static_cast<float*>(out),
                                                       T, d, k, c.status);
   }

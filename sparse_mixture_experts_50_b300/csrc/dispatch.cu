@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kRankThreads) dispatch_rank_kernel(const int32
                                                                      int32_t* __restrict__ offsets,
                                                                      int32_t* __restrict__ row_src,
                                                                      int32_t* __restrict__ slot_pos, int* status) {
+  pdl_enter();
   __shared__ int cnt[EMAX];
   __shared__ int cur[EMAX];
   __shared__ int wc[kRankThreads / 32][EMAX];
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const uint4
                                                                      const int32_t* __restrict__ row_src,
                                                                      uint4* __restrict__ x_perm, int Tk, int T,
                                                                      int vecs_per_row, int* status) {
+  pdl_enter();
   const long long total = static_cast<long long>(Tk) * vecs_per_row;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -114,9 +116,9 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const uint4
 cudaError_t launch_dispatch(const int32_t* idx, int Tk, int E, int k, int32_t* counts, int32_t* offsets,
                             int32_t* row_src, int32_t* slot_pos, const Ctx& c, cudaStream_t s) {
   if (E <= 8) {
-    dispatch_rank_kernel<8><<<1, kRankThreads, 0, s>>>(idx, Tk, E, k, counts, offsets, row_src, slot_pos, c.status);
+    launch_pdl(dispatch_rank_kernel<8>, 1, kRankThreads, 0, s, idx, Tk, E, k, counts, offsets, row_src, slot_pos, c.status);
   } else {
-    dispatch_rank_kernel<64><<<1, kRankThreads, 0, s>>>(idx, Tk, E, k, counts, offsets, row_src, slot_pos, c.status);
+    launch_pdl(dispatch_rank_kernel<64>, 1, kRankThreads, 0, s, idx, Tk, E, k, counts, offsets, row_src, slot_pos, c.status);
   }
   return cudaGetLastError();
 }
@@ -128,7 +130,7 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, void* x_pe
   const int cap = c.num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  gather_rows_kernel<<<static_cast<int>(blocks), kGatherThreads, 0, s>>>(static_cast<const uint4*>(x), row_src,
+  launch_pdl(gather_rows_kernel, static_cast<int>(blocks), kGatherThreads, 0, s, static_cast<const uint4*>(x), row_src,
                                                        static_cast<uint4*>(x_perm), Tk, T, vecs, c.status);
   return cudaGetLastError();
 }

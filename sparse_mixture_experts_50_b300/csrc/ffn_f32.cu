@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kThreads) ffn_f32_kernel(const float* __restri
                                                            const float* __restrict__ B0, const float* __restrict__ B1,
                                                            float* __restrict__ out, int Tk, int E, int K, int N,
                                                            int b_rows) {
+  pdl_enter();
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs0[BK][BN + 4];
   __shared__ float Bs1[BK][BN + 4];  // W3 tile (gate/up kernel only)
@@ -110,14 +111,14 @@ dim3 grid_for(int Tk, int E, int N) {
 cudaError_t launch_ffn_f32_gate_up(const float* x_perm, const int32_t* offsets, const float* W1, const float* W3,
                                    float* h, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s) {
   (void)c;
-  ffn_f32_kernel<true><<<grid_for(Tk, E, dff), kThreads, 0, s>>>(x_perm, offsets, W1, W3, h, Tk, E, d, dff, dff);
+  launch_pdl(ffn_f32_kernel<true>, grid_for(Tk, E, dff), kThreads, 0, s, x_perm, offsets, W1, W3, h, Tk, E, d, dff, dff);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ffn_f32_down(const float* h, const int32_t* offsets, const float* W2, float* y, int Tk, int d,
                                 int dff, int E, const Ctx& c, cudaStream_t s) {
   (void)c;
-  ffn_f32_kernel<false><<<grid_for(Tk, E, d), kThreads, 0, s>>>(h, offsets, W2, nullptr, y, Tk, E, dff, d, d);
+  launch_pdl(ffn_f32_kernel<false>, grid_for(Tk, E, d), kThreads, 0, s, h, offsets, W2, nullptr, y, Tk, E, dff, d, d);
   return cudaGetLastError();
 }
 

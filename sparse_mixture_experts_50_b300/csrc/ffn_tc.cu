@@ -24,6 +24,10 @@
 // raises a CTA-wide abort flag and records MOE_ETIMEOUT; each role then
 // leaves its loop, the producer waits (bounded) for its copies in flight, the
 // MMA warp waits (bounded) for its MMAs, and TMEM is freed before returning.
+//
+// The set-up (barriers, tensor-map prefetch, TMEM allocation) runs before the
+// kernel waits on its predecessor (programmatic dependent launch), so it
+// overlaps the previous kernel's tail.
 #include <cuda.h>
 #include <mutex>
 
@@ -116,6 +120,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int lane = threadIdx.x & 31;
   const volatile int* abort_flag = &ctl->abort_flag;
 
+  // Set-up that reads nothing the previous kernel writes: barriers, tensor
+  // maps, tensor memory.  It overlaps the previous kernel's tail.
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
@@ -127,6 +133,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     ptx::mbar_init(&ctl->drain, 1);
     ctl->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB0);
+    if (SWIGLU) ptx::prefetch_tmap(&tmB1);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  pdl_enter();
+  if (threadIdx.x == 0) {
     // Expert segments -> tile table.  A segment that is not inside [0, Tk]
     // or runs backwards is treated as empty and reported.
     int run = 0;
@@ -148,16 +167,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       run += mt * args.n_tiles;
       ctl->tile_prefix[e + 1] = run;
     }
-    ptx::fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&tmA);
-    ptx::prefetch_tmap(&tmB0);
-    if (SWIGLU) ptx::prefetch_tmap(&tmB1);
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
-    ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -369,6 +378,27 @@ int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows)
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
 }
 
+// Persistent grid size.  With many waves of tiles every SM is used.  With
+// only a few waves (small batches, where the kernel streams weights and is
+// bound by HBM), the last wave would leave most SMs idle while a few finish,
+// so the grid is shrunk (to no fewer than 3/4 of the SMs) to the size that
+// wastes the fewest tile slots in the last wave: 896 decode tiles run as
+// 7 x 128 rather than 6 x 148 + 8.
+int balanced_grid(long long tiles, int num_sms) {
+  if (tiles <= num_sms) return static_cast<int>(tiles < 1 ? 1 : tiles);
+  if (tiles >= 8LL * num_sms) return num_sms;
+  int best = num_sms;
+  long long best_waste = (tiles + num_sms - 1) / num_sms * num_sms - tiles;
+  for (int g = num_sms - 1; g * 4 >= num_sms * 3; --g) {
+    const long long waste = (tiles + g - 1) / g * g - tiles;
+    if (waste < best_waste) {
+      best = g;
+      best_waste = waste;
+    }
+  }
+  return best;
+}
+
 template <bool SWIGLU>
 int smem_attr_once(int device) {
   static std::mutex mu;
@@ -414,10 +444,11 @@ int launch_gemm(const void* A, const void* B0, const void* B1, const int32_t* of
   a.n_tiles = SWIGLU ? (n_out + BN_HALF - 1) / BN_HALF : (n_out + BN - 1) / BN;
   a.status = c.status;
   a.wait_ns = c.wait_ns;
-  // Upper bound on tiles: each expert may end in a partial row block.
-  const long long max_tiles = (static_cast<long long>(Tk) / BM + E) * a.n_tiles;
-  const int grid = static_cast<int>(max_tiles < c.num_sms ? max_tiles : c.num_sms);
-  grouped_gemm_tc_kernel<SWIGLU><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb0, tb1, a);
+  // Upper bound on tiles: whole row blocks plus at most one partial block
+  // per expert that has rows (at most min(E, Tk) of them).
+  const long long max_tiles = (static_cast<long long>(Tk) / BM + (E < Tk ? E : Tk)) * a.n_tiles;
+  const int grid = balanced_grid(max_tiles, c.num_sms);
+  launch_pdl(grouped_gemm_tc_kernel<SWIGLU>, grid, NUM_THREADS, SMEM_BYTES, s, ta, tb0, tb1, a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 

@@ -27,6 +27,7 @@ template <int EMAX, int TPT, typename TIn>
 __global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __restrict__ x, const TIn* __restrict__ Wg,
                                                                int T, int d, int E, int k, int32_t* __restrict__ idx,
                                                                float* __restrict__ w, float* __restrict__ logits) {
+  pdl_enter();
   constexpr int V = VecOf<TIn>::n;
   constexpr int WPT = TPT / 32;              // warps per token
   constexpr int TOK_PER_BLOCK = kThreads / TPT;
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __rest
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TIn* __restrict__ x, const TIn* __restrict__ gamma,
                                                            float eps, TIn* __restrict__ xn, int T, int d) {
+  pdl_enter();
   constexpr int V = VecOf<TIn>::n;
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -196,10 +198,10 @@ void launch_router_e(const TIn* xp, const TIn* gp, int T, int d, int E, int k, i
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   switch (tpt) {
-    case 32: router_topk_kernel<EMAX, 32, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits); break;
-    case 64: router_topk_kernel<EMAX, 64, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits); break;
-    case 128: router_topk_kernel<EMAX, 128, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits); break;
-    default: router_topk_kernel<EMAX, 256, TIn><<<grid, kThreads, 0, s>>>(xp, gp, T, d, E, k, idx, w, logits); break;
+    case 32: launch_pdl(router_topk_kernel<EMAX, 32, TIn>, grid, kThreads, 0, s, xp, gp, T, d, E, k, idx, w, logits); break;
+    case 64: launch_pdl(router_topk_kernel<EMAX, 64, TIn>, grid, kThreads, 0, s, xp, gp, T, d, E, k, idx, w, logits); break;
+    case 128: launch_pdl(router_topk_kernel<EMAX, 128, TIn>, grid, kThreads, 0, s, xp, gp, T, d, E, k, idx, w, logits); break;
+    default: launch_pdl(router_topk_kernel<EMAX, 256, TIn>, grid, kThreads, 0, s, xp, gp, T, d, E, k, idx, w, logits); break;
   }
 }
 
@@ -232,11 +234,11 @@ cudaError_t launch_rmsnorm(const void* x, const void* gamma, float eps, void* xn
                            const Ctx& c, cudaStream_t s) {
   const int grid = grid_for(T, c);
   if (dtype == MOE_DTYPE_BF16) {
-    rmsnorm_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+    launch_pdl(rmsnorm_kernel<__nv_bfloat16>, grid, kThreads, 0, s, static_cast<const __nv_bfloat16*>(x),
                                                             static_cast<const __nv_bfloat16*>(gamma), eps,
                                                             static_cast<__nv_bfloat16*>(xn), T, d);
   } else {
-    rmsnorm_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(x), static_cast<const float*>(gamma),
+    launch_pdl(rmsnorm_kernel<float>, grid, kThreads, 0, s, static_cast<const float*>(x), static_cast<const float*>(gamma),
                                                     eps, static_cast<float*>(xn), T, d);
   }
   return cudaGetLastError();
