@@ -306,26 +306,52 @@ def e2e_leg(layer, steps, warmup):
     return {"value": wl.T * steps / el, "unit": "tokens/s", "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb}
 
 
-def oracle_sample(name, max_tokens=None):
-    """Time the fp64 CPU oracle on a bounded sample of the workload."""
+def cpu_cores():
+    try:
+        import threadpoolctl
+        return int(max((i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()), default=1))
+    except Exception:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_time(name, tensors, tokens):
+    """Seconds the fp64 CPU oracle takes for the layer on `tokens` rows."""
     import oracle.moe_oracle as O
     wl = mw.get(name)
-    t = mw.make_inputs(wl)
-    n = wl.T if max_tokens is None else min(wl.T, max_tokens)
-    x = t["x"][:n]
+    t = tensors
+    x = t["x"][tokens]
     t0 = time.perf_counter()
     if wl.block:
         O.block_forward(x, t["gamma"], wl.eps, t["Wg"], t["W1"], t["W3"], t["W2"], wl.k)
     else:
         O.moe_forward(x, t["Wg"], t["W1"], t["W3"], t["W2"], wl.k)
-    el = time.perf_counter() - t0
-    try:
-        import threadpoolctl
-        cores = max((i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()), default=1)
-    except Exception:  # pragma: no cover
-        cores = os.cpu_count()
-    return {"value": n / el, "unit": "tokens/s", "cores": int(cores), "kind": "oracle",
-            "sample": f"{name}: first {n} of {wl.T} tokens, full layer in fp64 (numpy), {el:.1f} s"}
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(name, tensors, reps=3):
+    """The oracle, as it stands, on the whole workload batch `reps` times
+    (Mixtral decode: 16 tokens, ~4 s each on 8 cores)."""
+    wl = mw.get(name)
+    n = min(wl.T, 16)
+    times = [oracle_time(name, tensors, slice(0, n)) for _ in range(reps)]
+    el = statistics.median(times)
+    return {"value": n / el, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{name}: tokens 0-{n - 1} of {wl.T}, whole layer in fp64 (numpy), median of {reps} runs, "
+                      f"{el:.2f} s each"}
+
+
+def job_throughput(tokens_local, t_local, dist_on, device):
+    """Whole-job tokens/s: the tokens every rank processed over the slowest
+    rank's timed region (replicas: no collective touches the data path; this
+    all-reduce of two numbers is control only)."""
+    if not dist_on:
+        return tokens_local / t_local, t_local
+    import torch.distributed as dist
+    t = torch.tensor([t_local], dtype=torch.float64, device=device)
+    n = torch.tensor([tokens_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(n.item()) / float(t.item()), float(t.item())
 
 
 def config_of(name, n_gpus):
@@ -368,20 +394,30 @@ def main():
         names.insert(0, head_name)
 
     if args.impl == "reference":
+        # The fp64 CPU oracle timed on the host cores (rank 0 only).  Each
+        # step is a bounded sample: the whole batch when there are few steps,
+        # else 2 tokens (cycling through the batch), so any --steps run ends
+        # within minutes.  Warm-up steps evaluate 1 token.
         if rank != 0:
             return
+        wl = mw.get(head_name)
         t0 = time.perf_counter()
-        samples = []
-        for _ in range(args.warmup):
-            pass  # the oracle has no warm-up state; each step is a fresh evaluation
-        for _ in range(max(1, min(args.steps, 3))):
-            samples.append(oracle_sample(head_name))
-        v = statistics.median(s["value"] for s in samples)
+        tensors = make_tensors(wl, {})
+        per = wl.T if args.steps <= 4 else min(2, wl.T)
+        for i in range(args.warmup):
+            oracle_time(head_name, tensors, slice(i % wl.T, i % wl.T + 1))
+        el = 0.0
+        for i in range(args.steps):
+            a = (i * per) % wl.T
+            el += oracle_time(head_name, tensors, slice(a, min(a + per, wl.T)))
+        v = per * args.steps / el
+        base = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                "sample": f"{head_name}: {per} token(s) per step, whole layer in fp64 (numpy)"}
         line = {"metric": METRIC, "value": v, "unit": "tokens/s", "impl": "reference", "n_gpus": 1,
-                "steps": len(samples), "warmup": args.warmup, "ms_per_step": 1e3 * mw.get(head_name).T / v,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config_of(head_name, 1),
-                "cpu_baseline": {**samples[0], "value": v},
+                "data": "synthetic", "config": {**config_of(head_name, 1), "l2": "not applicable (host CPU)"},
+                "cpu_baseline": base,
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "wall_s": time.perf_counter() - t0}
         print(json.dumps(line), flush=True)
@@ -415,21 +451,18 @@ def main():
     head = results[head_name]
     # Whole job: tokens of all ranks over the slowest rank's timed region.
     t_local = head["ms_per_step"] * args.steps * 1e-3
-    t_max = t_local
-    if dist_on:
-        tt = torch.tensor([t_local], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(tt.item())
-    value = world * mw.get(head_name).T * args.steps / t_max
+    value, _ = job_throughput(mw.get(head_name).T * args.steps, t_local, dist_on, device)
 
     e2e = None if args.no_e2e else e2e_leg(head_layer, args.steps, args.warmup)
     if dist_on and e2e is not None:
-        tt = torch.tensor([e2e["value"]], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MIN)
-        e2e["value"] = float(tt.item()) * world
+        # every rank ran the same number of host-timed steps
+        T = mw.get(head_name).T
+        e2e["value"], _ = job_throughput(T * args.steps, T * args.steps / e2e["value"], True, device)
 
     if rank == 0:
-        cpu = None if (args.no_cpu_baseline or dist_on) else oracle_sample(head_name)
+        cpu = None
+        if not (args.no_cpu_baseline or dist_on):
+            cpu = cpu_baseline(head_name, make_tensors(mw.get(head_name), shared))
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
