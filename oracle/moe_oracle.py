@@ -215,3 +215,43 @@ def moe_layer_active_param_count(d, F, E, k) -> int:
     """Parameters one token touches in an MoE layer: k experts and the gate."""
     per_expert = sum(a * b for a, b in expert_param_shapes(d, F))
     return k * per_expert + d * E
+
+
+# ---------------------------------------------------------------- int8 weight-only experts
+# KerasFormers Mixtral docs, "Lower memory": checkpoints may be loaded with
+# the weights alone quantized to int8 while activations stay bf16.  The docs
+# do not spell the scheme out; the reading taken here is the plain one for a
+# weight-only int8 linear map: symmetric, one fp32 scale per output channel
+# (per row of the nn.Linear weight), scale = max|row| / 127, codes rounded to
+# nearest (ties to even) and clamped to [-127, 127].  The codes are integers
+# decided by floating point, so they are decided in fp32 (IEEE division, as a
+# GPU kernel computes them): s = fl32(amax / 127), q = rint(fl32(w / s)).
+# A row of zeros has scale 0 and codes 0.
+def quantize_int8_rows(W):
+    """Per-row symmetric int8 quantisation of W[..., cols].
+
+    Returns (q int8 with W's shape, s float32 with W's shape minus the last
+    axis)."""
+    w32 = f64(W).astype(np.float32)
+    amax = np.max(np.abs(w32), axis=-1)
+    s = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    q = np.rint((w32 / safe[..., None]).astype(np.float32))
+    q = np.clip(q, -127, 127)
+    q = np.where(s[..., None] > 0, q, 0.0)
+    return q.astype(np.int8), s
+
+
+def dequantize_int8_rows(q, s) -> np.ndarray:
+    """The weight a quantised layer multiplies by: s[row] * q[row, col], exact in fp64."""
+    return np.asarray(q, dtype=np.float64) * np.asarray(s, dtype=np.float64)[..., None]
+
+
+def moe_forward_w8(x, Wg, q1, s1, q3, s3, q2, s2, k):
+    """The sparse MoE layer with int8 expert weights: the router uses Wg as
+    given; every expert matrix is its dequantised value s * q.  Returns
+    (out[T,d], w[T,k], idx[T,k], logits[T,E])."""
+    W1 = dequantize_int8_rows(q1, s1)
+    W3 = dequantize_int8_rows(q3, s3)
+    W2 = dequantize_int8_rows(q2, s2)
+    return moe_forward(x, Wg, W1, W3, W2, k)

@@ -392,4 +392,112 @@ def pin_parameter_counts_match_pages(o):
     assert o.moe_layer_param_count(d, F, E) == 1_409_318_912
 
 
+# ------------------------------------------------------------------ int8 weight-only experts
+# KerasFormers Mixtral docs, "Lower memory": weights alone quantised to int8.
+# Reading: symmetric, one scale per output row, s = max|row| / 127, codes
+# rounded half to even and clamped to [-127, 127].
+def _bf16_rows(seed, rows, cols, scale=0.02):
+    r = _rng(seed)
+    w = torch.from_numpy(r.standard_normal((rows, cols)) * scale).to(torch.bfloat16)
+    return w.to(torch.float64).numpy()
+
+
+def pin_int8_hand_values(o):
+    """Hand-worked rows (tests/golden/int8_rows_hand.json): ties to even, the
+    127 divisor, a zero row."""
+    with open(os.path.join(GOLDEN, "int8_rows_hand.json")) as f:
+        rows = json.load(f)["rows"]
+    for row in rows:
+        q, s = o.quantize_int8_rows(np.array([row["w"]]))
+        assert q.dtype == np.int8
+        assert q[0].tolist() == row["q"], (row["w"], q[0].tolist())
+        assert float(s[0]) == row["scale"], (row["w"], float(s[0]))
+
+
+def pin_int8_exact_rational(o):
+    """Every code is the integer nearest to w / s computed in exact rational
+    arithmetic (ties to even), except where w / s lies within fp32 rounding of
+    a midpoint; the scale is max|row| / 127 to fp32 rounding; the amax
+    element gets +-127 with its sign."""
+    from fractions import Fraction
+    W = _bf16_rows(81, 24, 40)
+    W[3] = 0.0
+    q, s = o.quantize_int8_rows(W)
+    assert q.shape == W.shape and s.shape == (24,)
+    for i in range(W.shape[0]):
+        amax = max(abs(Fraction(float(v))) for v in W[i])
+        if amax == 0:
+            assert s[i] == 0 and not q[i].any()
+            continue
+        si = Fraction(float(s[i]))
+        assert abs(si - amax / 127) <= amax / 127 * Fraction(1, 1 << 23), i
+        j = int(np.argmax(np.abs(W[i])))
+        assert int(q[i, j]) == (127 if W[i, j] > 0 else -127), i
+        for c in range(W.shape[1]):
+            v = Fraction(float(W[i, c])) / si
+            n = math.floor(v)
+            frac = v - n
+            if abs(frac - Fraction(1, 2)) <= abs(v) * Fraction(1, 1 << 22):
+                assert int(q[i, c]) in (n, n + 1), (i, c)
+                continue
+            want = n + 1 if frac > Fraction(1, 2) else n
+            want = max(-127, min(127, want))
+            assert int(q[i, c]) == want, (i, c, float(v), int(q[i, c]))
+
+
+def pin_int8_error_bound(o):
+    """|w - s q| <= s / 2 (plus fp32 rounding of the quotient) for every
+    element, |q| <= 127, on Mixtral-like rows of 4096."""
+    W = _bf16_rows(83, 16, 4096)
+    q, s = o.quantize_int8_rows(W)
+    assert np.all(np.abs(q.astype(np.int64)) <= 127)
+    err = np.abs(W - q.astype(np.float64) * s.astype(np.float64)[:, None])
+    assert np.all(err <= s[:, None] * (0.5 + 127 * 2.0 ** -23))
+    assert np.all(np.abs(o.dequantize_int8_rows(q, s) - W) <= s[:, None] * (0.5 + 127 * 2.0 ** -23))
+
+
+def pin_int8_symmetry_scaling_rows(o):
+    """Negating w negates q; scaling a row by 2^j scales s by 2^j and keeps q;
+    each row is quantised on its own (per output channel, not per column)."""
+    W = _bf16_rows(85, 12, 64)
+    q, s = o.quantize_int8_rows(W)
+    qn, sn = o.quantize_int8_rows(-W)
+    assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+    for j in (-3, 5):
+        qj, sj = o.quantize_int8_rows(W * 2.0 ** j)
+        assert np.array_equal(qj, q) and np.array_equal(sj, (s * np.float32(2.0 ** j)).astype(np.float32))
+    for i in range(12):
+        qi, si = o.quantize_int8_rows(W[i:i + 1])
+        assert np.array_equal(qi[0], q[i]) and si[0] == s[i]
+    W3 = np.stack([W, 4.0 * W])
+    q3, s3 = o.quantize_int8_rows(W3)
+    assert np.array_equal(q3[0], q) and np.array_equal(q3[1], q) and np.array_equal(s3[1], 4 * s)
+
+
+def pin_w8_layer_brute_force(o):
+    """The int8-weight layer is the layer of the dequantised weights s * q,
+    checked token by token with pure-Python loops; and it stays within the
+    quantisation error of the unquantised layer."""
+    L = _tiny_layer(87, T=8, d=12, F=10, E=4)
+    q1, s1 = o.quantize_int8_rows(L["W1"])
+    q3, s3 = o.quantize_int8_rows(L["W3"])
+    q2, s2 = o.quantize_int8_rows(L["W2"])
+    out, w, idx, _ = o.moe_forward_w8(L["x"], L["Wg"], q1, s1, q3, s3, q2, s2, 2)
+
+    def deq(q, s, e):
+        return [[float(s[e, r]) * int(q[e, r, c]) for c in range(q.shape[2])] for r in range(q.shape[1])]
+
+    for t in range(8):
+        logits = [_py_dot(L["x"][t], L["Wg"][e]) for e in range(4)]
+        top = sorted(range(4), key=lambda e: -logits[e])[:2]
+        z = [math.exp(logits[e] - logits[top[0]]) for e in top]
+        want = [0.0] * 12
+        for j, e in enumerate(top):
+            y = _py_swiglu(L["x"][t], deq(q1, s1, e), deq(q3, s3, e), deq(q2, s2, e))
+            want = [a + z[j] / sum(z) * b for a, b in zip(want, y)]
+        assert np.allclose(out[t], want, rtol=1e-12, atol=1e-14), t
+    ref, _, _, _ = o.moe_forward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 2)
+    assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 0.03
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

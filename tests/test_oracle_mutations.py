@@ -156,12 +156,56 @@ def _two_matrix_expert(m):
     m.expert_param_shapes = lambda d, F: [(F, d), (d, F)]
 
 
+def _int8_divisor_128(m):
+    def quant(W):
+        w32 = m.f64(W).astype(np.float32)
+        s = (np.max(np.abs(w32), axis=-1) / np.float32(128.0)).astype(np.float32)
+        safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+        q = np.clip(np.rint(w32 / safe[..., None]), -127, 127)
+        return q.astype(np.int8), s
+    m.quantize_int8_rows = quant
+
+
+def _int8_truncates(m):
+    def quant(W):
+        w32 = m.f64(W).astype(np.float32)
+        s = (np.max(np.abs(w32), axis=-1) / np.float32(127.0)).astype(np.float32)
+        safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+        return np.trunc(w32 / safe[..., None]).astype(np.int8), s
+    m.quantize_int8_rows = quant
+
+
+def _int8_ties_away_from_zero(m):
+    def quant(W):
+        w32 = m.f64(W).astype(np.float32)
+        s = (np.max(np.abs(w32), axis=-1) / np.float32(127.0)).astype(np.float32)
+        safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+        v = w32 / safe[..., None]
+        return (np.sign(v) * np.floor(np.abs(v) + 0.5)).astype(np.int8), s
+    m.quantize_int8_rows = quant
+
+
+def _int8_per_column(m):
+    def quant(W):
+        w32 = m.f64(W).astype(np.float32)
+        s = (np.max(np.abs(w32), axis=-2) / np.float32(127.0)).astype(np.float32)
+        safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+        q = np.clip(np.rint(w32 / safe[..., None, :]), -127, 127)
+        return q.astype(np.int8), np.max(s, axis=-1) * np.ones(w32.shape[:-1], np.float32)
+    m.quantize_int8_rows = quant
+
+
+def _w8_drops_scale(m):
+    m.dequantize_int8_rows = lambda q, s: np.asarray(q, dtype=np.float64)
+
+
 MUTANTS = {f.__name__[1:]: f for f in [
     _swap_gate_up, _silu_sign, _silu_is_sigmoid, _no_renormalise, _ascending_topk,
     _ties_to_higher_index, _drop_gate_weight, _only_first_slot, _transposed_down,
     _gate_transposed, _rms_no_square, _rms_no_eps, _rms_no_gamma, _bf16_truncates,
     _block_no_residual, _block_unnormalised, _two_matrix_expert, _dispatch_unstable,
-    _dispatch_token_not_pair, _hidden_no_gate, _rms32_no_square]}
+    _dispatch_token_not_pair, _hidden_no_gate, _rms32_no_square, _int8_divisor_128, _int8_truncates,
+    _int8_ties_away_from_zero, _int8_per_column, _w8_drops_scale]}
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
