@@ -46,7 +46,7 @@ import moe_workloads as mw  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (Mixtral 4096/14336, E8 k2, bf16) + % of roofline"
 HEADLINE = "decode"
-ALL_BENCH = ["decode", "prefill", "skewed", "skewed_zero", "block"]
+ALL_BENCH = ["decode", "prefill", "skewed", "skewed_zero", "block", "decode_w8", "prefill_w8"]
 L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = {False: 6, True: 7}  # router, rank, gather, gate_up, down, combine (+ rmsnorm)
 
@@ -74,9 +74,13 @@ def algorithmic(wl, counts):
     T, d, F, E, k = wl.T, wl.d, wl.F, wl.E, wl.k
     used = int(sum(1 for c in counts if c > 0))
     flops = T * (k * 6 * d * F + 2 * d * E)
-    nbytes = used * 3 * d * F * 2 + d * E * 2 + 2 * T * d * 2 + (d * 2 if wl.block else 0)
+    if wl.w8:  # int8 codes + one fp32 scale per row
+        expert_bytes, gu_expert_bytes = 3 * d * F + (2 * F + d) * 4, 2 * d * F + 2 * F * 4
+    else:
+        expert_bytes, gu_expert_bytes = 3 * d * F * 2, 2 * d * F * 2
+    nbytes = used * expert_bytes + d * E * 2 + 2 * T * d * 2 + (d * 2 if wl.block else 0)
     gu_flops = T * k * 4 * d * F
-    gu_bytes = used * 2 * d * F * 2
+    gu_bytes = used * gu_expert_bytes
     return flops, nbytes, gu_flops, gu_bytes
 
 
@@ -177,6 +181,13 @@ class Layer:
         g = {n: v.to(dev, non_blocking=False) for n, v in tensors.items()}
         self.x, self.Wg, self.W1, self.W3, self.W2 = g["x"], g["Wg"], g["W1"], g["W3"], g["W2"]
         self.gamma = g.get("gamma")
+        if wl.w8:
+            # Weight preparation (once, outside any timed region): per-row
+            # int8 codes and fp32 scales on the GPU; the bf16 copies go.
+            self.W1q, self.W1s = B.moe_quantize_int8(self.W1)
+            self.W3q, self.W3s = B.moe_quantize_int8(self.W3)
+            self.W2q, self.W2s = B.moe_quantize_int8(self.W2)
+            self.W1 = self.W3 = self.W2 = None
         dt = wl.torch_dtype
         self.xn = torch.empty((T, d), dtype=dt, device=dev) if wl.block else None
         self.idx = torch.empty((T, k), dtype=torch.int32, device=dev)
@@ -202,10 +213,16 @@ class Layer:
         B.moe_permute(xin, self.idx, wl.E, out=(self.counts, self.offsets, self.row_src, self.slot_pos, self.x_perm))
         if ev is not None:
             ev[1].record()
-        B.moe_expert_gate_up(self.x_perm, self.offsets, self.W1, self.W3, self.h)
+        if wl.w8:
+            B.moe_expert_gate_up_w8(self.x_perm, self.offsets, self.W1q, self.W1s, self.W3q, self.W3s, self.h)
+        else:
+            B.moe_expert_gate_up(self.x_perm, self.offsets, self.W1, self.W3, self.h)
         if ev is not None:
             ev[2].record()
-        B.moe_expert_down(self.h, self.offsets, self.W2, self.y)
+        if wl.w8:
+            B.moe_expert_down_w8(self.h, self.offsets, self.W2q, self.W2s, self.y)
+        else:
+            B.moe_expert_down(self.h, self.offsets, self.W2, self.y)
         if ev is not None:
             ev[3].record()
         B.moe_combine(self.y, self.slot_pos, self.w, wl.T, residual=self.x if wl.block else None, out=self.out)
@@ -281,7 +298,7 @@ def bench_workload(name, shared, args, device, peaks, dist_on):
         "kernel_ms": {p: sum(v) / len(v) for p, v in parts.items()},
         "expert_counts": counts,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "kernel": "grouped_gemm_tc_kernel<gate_up+SwiGLU>",
+                     "kernel": "grouped_gemm_tc_kernel<gate_up+SwiGLU%s>" % (", int8 weights" if wl.w8 else ""),
                      "algorithmic_per_launch": gu_bytes if bound == "hbm" else gu_flops,
                      "traffic": ncu_traffic(name)},
         "wall_s": wall,
@@ -357,6 +374,7 @@ def job_throughput(tokens_local, t_local, dist_on, device):
 def config_of(name, n_gpus):
     wl = mw.get(name)
     return {"workload": f"{name}: T={wl.T}, d={wl.d}, d_ff={wl.F}, E={wl.E}, top-{wl.k}, {wl.dtype}"
+                        + (", int8 weight-only experts" if wl.w8 else "")
                         + (", RMSNorm + residual" if wl.block else "")
                         + (", skewed expert load" if wl.skew else ""),
             "T": wl.T, "d": wl.d, "d_ff": wl.F, "E": wl.E, "k": wl.k,
@@ -378,7 +396,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workloads", default=",".join(ALL_BENCH))
-    ap.add_argument("--headline", default=HEADLINE, choices=ALL_BENCH,
+    ap.add_argument("--headline", default=HEADLINE, choices=[n for n in ALL_BENCH if not mw.get(n).w8],
                     help="workload of the JSON line's value (default: Mixtral-shape decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

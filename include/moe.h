@@ -189,6 +189,58 @@ int moe_forward_host(const void* x_host, const void* Wg, const void* W1, const v
                      int dtype, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * ---- int8 weight-only expert weights ------------------------------------
+ * KerasFormers Mixtral docs, "Lower memory": the weights alone may be
+ * quantised to int8 while activations stay bf16.  The docs do not give the
+ * scheme; this library uses symmetric per-output-channel codes: each row of
+ * an nn.Linear weight W[rows, cols] (W1/W3: rows = E*dff, cols = d; W2:
+ * rows = E*d, cols = dff) gets one fp32 scale s = max|row| / 127 and codes
+ * q = round-half-even(w / s) clamped to [-127, 127] (both divisions IEEE
+ * fp32, so the codes are reproducible bit for bit); a zero row has s = 0 and
+ * q = 0.  The layer then uses s[row] * q[row, col] in place of W.  The expert
+ * weights take half the bytes of bf16 (plus 4 bytes per row), which is what
+ * bounds the layer at small batches.  The router's Wg stays bf16.
+ */
+
+/*
+ * Quantise a bf16 matrix W[rows, cols] (device) to q[rows, cols] int8 and
+ * scale[rows] fp32 (device, caller-owned).  cols % 8 == 0; W and q 16-byte
+ * aligned.  Inputs are expected finite.
+ */
+int moe_quantize_int8(const void* W, int rows, int cols, int8_t* q, float* scale, moe_stream_t stream);
+
+/*
+ * Step a4 with int8 weights: as moe_expert_gate_up (bf16 x_perm and h_perm),
+ * with W1q/W3q [E,dff,d] int8 and W1s/W3s [E*dff] fp32 row scales:
+ *   h_perm[p,f] = silu(W1s[e,f] * sum_c x_perm[p,c] W1q[e,f,c])
+ *                 * (W3s[e,f] * sum_c x_perm[p,c] W3q[e,f,c])
+ * fp32 accumulation, h rounded once to bf16.  All pointers 16-byte aligned.
+ */
+int moe_expert_gate_up_w8(const void* x_perm, const int32_t* offsets, const int8_t* W1q, const float* W1s,
+                          const int8_t* W3q, const float* W3s, void* h_perm, int Tk, int d, int dff, int E,
+                          moe_stream_t stream);
+
+/*
+ * Step a5 with int8 weights: y_perm[p,c] = W2s[e,c] * sum_f h_perm[p,f] W2q[e,c,f],
+ * W2q [E,d,dff] int8, W2s [E*d] fp32; bf16 h_perm / y_perm.
+ */
+int moe_expert_down_w8(const void* h_perm, const int32_t* offsets, const int8_t* W2q, const float* W2s,
+                       void* y_perm, int Tk, int d, int dff, int E, moe_stream_t stream);
+
+/*
+ * The whole bf16 layer with int8 expert weights (a1..a6).  x[T,d], Wg[E,d],
+ * out[T,d] bf16; the six weight arguments as above.  _ws takes caller scratch
+ * of moe_forward_workspace_bytes(T, d, dff, E, k, MOE_DTYPE_BF16) bytes
+ * (256-byte aligned); the other takes it from cudaMallocAsync on `stream`.
+ */
+int moe_forward_w8_ws(const void* x, const void* Wg, const int8_t* W1q, const float* W1s, const int8_t* W3q,
+                      const float* W3s, const int8_t* W2q, const float* W2s, void* out, int T, int d, int dff,
+                      int E, int k, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+int moe_forward_w8(const void* x, const void* Wg, const int8_t* W1q, const float* W1s, const int8_t* W3q,
+                   const float* W3s, const int8_t* W2q, const float* W2s, void* out, int T, int d, int dff, int E,
+                   int k, moe_stream_t stream);
+
+/*
  * Scratch size built into moe_forward_noalloc (16 MiB per GPU).
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)

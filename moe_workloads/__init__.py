@@ -66,6 +66,7 @@ class Workload:
     block: bool = False  # RMSNorm prologue + residual epilogue
     eps: float = RMSNORM_EPS
     bias_key: str | None = None  # skew_bias.json entry (default: name)
+    w8: bool = False  # expert weights quantised to int8 (per-row scales) before use
 
     @property
     def Tk(self) -> int:
@@ -91,6 +92,11 @@ WORKLOADS = {
     "skewed": _mixtral("skewed", 8192, skew="shares"),
     "skewed_zero": _mixtral("skewed_zero", 8192, skew="zero", bias_key="skewed"),
     "block": _mixtral("block", 8192, block=True),
+    # The same decode and prefill batches with int8 weight-only experts
+    # (KerasFormers Mixtral docs, "Lower memory"); the bf16 weights drawn
+    # here are quantised per row before the layer runs.
+    "decode_w8": _mixtral("decode_w8", 16, w8=True),
+    "prefill_w8": _mixtral("prefill_w8", 4096, w8=True),
 }
 
 # Reduced sizes with the same structure, small enough for the oracle to finish

@@ -47,6 +47,11 @@ SIGNATURES = {
     "moe_block_forward": (_I, [_P, _P, _F, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_forward_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "moe_quantize_int8": (_I, [_P, _I, _I, _P, _P, _P]),
+    "moe_expert_gate_up_w8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "moe_expert_down_w8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "moe_forward_w8_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "moe_forward_w8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_get_device_status": (_I, [_P, ctypes.POINTER(_I), _I]),
     "moe_set_wait_limit_ns": (_I, [_LL]),
@@ -295,6 +300,73 @@ def moe_forward_host(x_host, Wg, W1, W3, W2, k, ws, out_host=None, stream=None):
                                                       dff, E, k, _dtype(x_host), _p(ws), ws.numel(),
                                                       _stream(stream)))
     return out_host
+
+
+# ------------------------------------------------------------------ int8 weights
+def moe_quantize_int8(W, q=None, scale=None, stream=None):
+    """Per-row int8 quantisation of a bf16 matrix (any leading shape, rows =
+    product of the leading dims): returns (q int8 like W, scale fp32 [rows])."""
+    _dev(W, q, scale)
+    if W.dtype != torch.bfloat16:
+        raise TypeError("moe_quantize_int8 takes a bfloat16 matrix")
+    cols = W.shape[-1]
+    rows = W.numel() // cols
+    if q is None:
+        q = torch.empty(W.shape, dtype=torch.int8, device=W.device)
+    if scale is None:
+        scale = torch.empty(W.shape[:-1], dtype=torch.float32, device=W.device)
+    _check("moe_quantize_int8", lib().moe_quantize_int8(_p(W), rows, cols, _p(q), _p(scale), _stream(stream)))
+    return q, scale
+
+
+def moe_expert_gate_up_w8(x_perm, offsets, W1q, W1s, W3q, W3s, h_perm=None, stream=None):
+    """Step a4 with int8 weights: returns h_perm[Tk,dff] (bf16)."""
+    _dev(x_perm, offsets, W1q, W1s, W3q, W3s, h_perm)
+    Tk, d = x_perm.shape
+    E, dff, _ = W1q.shape
+    if h_perm is None:
+        h_perm = torch.empty((Tk, dff), dtype=x_perm.dtype, device=x_perm.device)
+    _check("moe_expert_gate_up_w8", lib().moe_expert_gate_up_w8(_p(x_perm), _p(offsets), _p(W1q), _p(W1s), _p(W3q),
+                                                                _p(W3s), _p(h_perm), Tk, d, dff, E,
+                                                                _stream(stream)))
+    return h_perm
+
+
+def moe_expert_down_w8(h_perm, offsets, W2q, W2s, y_perm=None, stream=None):
+    """Step a5 with int8 weights: returns y_perm[Tk,d] (bf16)."""
+    _dev(h_perm, offsets, W2q, W2s, y_perm)
+    Tk, dff = h_perm.shape
+    E, d, _ = W2q.shape
+    if y_perm is None:
+        y_perm = torch.empty((Tk, d), dtype=h_perm.dtype, device=h_perm.device)
+    _check("moe_expert_down_w8", lib().moe_expert_down_w8(_p(h_perm), _p(offsets), _p(W2q), _p(W2s), _p(y_perm), Tk,
+                                                          d, dff, E, _stream(stream)))
+    return y_perm
+
+
+def moe_forward_w8_ws(x, Wg, W1q, W1s, W3q, W3s, W2q, W2s, k, ws, out=None, stream=None):
+    """The bf16 layer with int8 expert weights on caller scratch `ws`."""
+    _dev(x, Wg, W1q, W1s, W3q, W3s, W2q, W2s, ws, out)
+    T, d = x.shape
+    E, dff, _ = W1q.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check("moe_forward_w8_ws", lib().moe_forward_w8_ws(_p(x), _p(Wg), _p(W1q), _p(W1s), _p(W3q), _p(W3s), _p(W2q),
+                                                        _p(W2s), _p(out), T, d, dff, E, k, _p(ws), ws.numel(),
+                                                        _stream(stream)))
+    return out
+
+
+def moe_forward_w8(x, Wg, W1q, W1s, W3q, W3s, W2q, W2s, k, out=None, stream=None):
+    """The bf16 layer with int8 expert weights, one call."""
+    _dev(x, Wg, W1q, W1s, W3q, W3s, W2q, W2s, out)
+    T, d = x.shape
+    E, dff, _ = W1q.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check("moe_forward_w8", lib().moe_forward_w8(_p(x), _p(Wg), _p(W1q), _p(W1s), _p(W3q), _p(W3s), _p(W2q),
+                                                  _p(W2s), _p(out), T, d, dff, E, k, _stream(stream)))
+    return out
 
 
 def moe_forward_noalloc(x, Wg, W1, W3, W2, k, out=None, stream=None):

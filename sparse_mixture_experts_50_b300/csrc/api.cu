@@ -120,6 +120,16 @@ int ffn_down(const void* h, const int32_t* offsets, const void* W2, void* y, int
                                        static_cast<float*>(y), Tk, d, dff, E, c, s));
 }
 
+// int8 expert weights (codes + per-row scales) for the weight-only path.
+struct W8Weights {
+  const int8_t* q1;
+  const float* s1;
+  const int8_t* q3;
+  const float* s3;
+  const int8_t* q2;
+  const float* s2;
+};
+
 struct WsLayout {
   size_t idx, w, counts, offs, row_src, slot_pos, x_perm, h, y, xn, total;
 };
@@ -145,10 +155,11 @@ WsLayout ws_layout(int T, int d, int dff, int E, int k, int dtype) {
   return L;
 }
 
-// The layer on caller scratch; gamma != NULL selects the block form.
+// The layer on caller scratch; gamma != NULL selects the block form, w8 !=
+// NULL the int8 expert weights (W1, W3, W2 are then unused).
 int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, const void* W1, const void* W3,
                  const void* W2, void* out, int T, int d, int dff, int E, int k, int dtype, void* ws, size_t ws_bytes,
-                 const Ctx& c, cudaStream_t s) {
+                 const Ctx& c, cudaStream_t s, const W8Weights* w8 = nullptr) {
   const WsLayout L = ws_layout(T, d, dff, E, k, dtype);
   if (ws_bytes < L.total) return MOE_ENOMEM;
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -171,8 +182,13 @@ int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, co
   MOE_TRY(launch_rc(launch_router(xin, Wg, T, d, E, k, idx, w, nullptr, dtype, c, s)));
   MOE_TRY(launch_rc(launch_dispatch(idx, Tk, E, k, counts, offs, row_src, slot_pos, c, s)));
   MOE_TRY(launch_rc(launch_gather_rows(xin, row_src, x_perm, T, Tk, static_cast<size_t>(d) * esize(dtype), c, s)));
-  MOE_TRY(ffn_gate_up(x_perm, offs, W1, W3, h, Tk, d, dff, E, dtype, c, s));
-  MOE_TRY(ffn_down(h, offs, W2, y, Tk, d, dff, E, dtype, c, s));
+  if (w8 != nullptr) {
+    MOE_TRY(launch_w8_gate_up(x_perm, offs, w8->q1, w8->s1, w8->q3, w8->s3, h, Tk, d, dff, E, c, s));
+    MOE_TRY(launch_w8_down(h, offs, w8->q2, w8->s2, y, Tk, d, dff, E, c, s));
+  } else {
+    MOE_TRY(ffn_gate_up(x_perm, offs, W1, W3, h, Tk, d, dff, E, dtype, c, s));
+    MOE_TRY(ffn_down(h, offs, W2, y, Tk, d, dff, E, dtype, c, s));
+  }
   MOE_TRY(launch_rc(launch_combine(y, slot_pos, w, gamma != nullptr ? x : nullptr, out, T, d, k, dtype, c, s)));
   return MOE_OK;
 }
@@ -209,6 +225,41 @@ int forward_alloc(const void* x, const void* gamma, float eps, const void* Wg, c
 }
 
 int check_eps(float eps) { return (std::isfinite(eps) && eps >= 0.0f) ? MOE_OK : MOE_EINVAL; }
+
+int check_w8(const W8Weights& w) {
+  const void* ptrs[] = {w.q1, w.s1, w.q3, w.s3, w.q2, w.s2};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
+  return MOE_OK;
+}
+
+int forward_w8(const void* x, const void* Wg, const W8Weights& w8, void* out, int T, int d, int dff, int E, int k,
+               void* ws, size_t ws_bytes, bool alloc, cudaStream_t s) {
+  MOE_TRY(check_tokens(T, d, E, k, MOE_DTYPE_BF16));
+  MOE_TRY(check_ffn(T * k, d, dff, E, MOE_DTYPE_BF16));
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || Wg == nullptr || out == nullptr || !aligned(x, 16) || !aligned(Wg, 16) || !aligned(out, 16))
+    return MOE_EINVAL;
+  MOE_TRY(check_w8(w8));
+  if (!alloc && (ws == nullptr || !aligned(ws, 256))) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(out, &c));
+  if (!alloc) {
+    return forward_impl(x, nullptr, 0.0f, Wg, nullptr, nullptr, nullptr, out, T, d, dff, E, k, MOE_DTYPE_BF16, ws,
+                        ws_bytes, c, s, &w8);
+  }
+  const size_t bytes = ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16).total;
+  void* buf = nullptr;
+  if (cudaMallocAsync(&buf, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ENOMEM;
+  }
+  const int rc = forward_impl(x, nullptr, 0.0f, Wg, nullptr, nullptr, nullptr, out, T, d, dff, E, k, MOE_DTYPE_BF16,
+                              buf, bytes, c, s, &w8);
+  const cudaError_t fe = cudaFreeAsync(buf, s);
+  if (rc != MOE_OK) return rc;
+  return fe == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
 
 }  // namespace
 }  // namespace moe
@@ -394,6 +445,55 @@ int moe_forward_host(const void* x_host, const void* Wg, const void* W1, const v
                        stream));
   if (cudaMemcpyAsync(out_host, out_dev, act_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MOE_ECUDA;
   return cudaStreamSynchronize(stream) == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
+
+int moe_quantize_int8(const void* W, int rows, int cols, int8_t* q, float* scale, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0) return MOE_EINVAL;
+  if (cols % 8 != 0) return MOE_EUNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (!W || !q || !scale || !aligned(W, 16) || !aligned(q, 16) || !aligned(scale, 4)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(q, &c));
+  return launch_rc(launch_quantize_int8(W, rows, cols, q, scale, c, stream));
+}
+
+int moe_expert_gate_up_w8(const void* x_perm, const int32_t* offsets, const int8_t* W1q, const float* W1s,
+                          const int8_t* W3q, const float* W3s, void* h_perm, int Tk, int d, int dff, int E,
+                          moe_stream_t stream) {
+  MOE_TRY(check_ffn(Tk, d, dff, E, MOE_DTYPE_BF16));
+  if (Tk == 0) return MOE_OK;
+  const void* ptrs[] = {x_perm, offsets, W1q, W1s, W3q, W3s, h_perm};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(h_perm, &c));
+  return launch_w8_gate_up(x_perm, offsets, W1q, W1s, W3q, W3s, h_perm, Tk, d, dff, E, c, stream);
+}
+
+int moe_expert_down_w8(const void* h_perm, const int32_t* offsets, const int8_t* W2q, const float* W2s, void* y_perm,
+                       int Tk, int d, int dff, int E, moe_stream_t stream) {
+  MOE_TRY(check_ffn(Tk, d, dff, E, MOE_DTYPE_BF16));
+  if (Tk == 0) return MOE_OK;
+  const void* ptrs[] = {h_perm, offsets, W2q, W2s, y_perm};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(y_perm, &c));
+  return launch_w8_down(h_perm, offsets, W2q, W2s, y_perm, Tk, d, dff, E, c, stream);
+}
+
+int moe_forward_w8_ws(const void* x, const void* Wg, const int8_t* W1q, const float* W1s, const int8_t* W3q,
+                      const float* W3s, const int8_t* W2q, const float* W2s, void* out, int T, int d, int dff, int E,
+                      int k, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  const W8Weights w8{W1q, W1s, W3q, W3s, W2q, W2s};
+  return forward_w8(x, Wg, w8, out, T, d, dff, E, k, workspace, workspace_bytes, false, stream);
+}
+
+int moe_forward_w8(const void* x, const void* Wg, const int8_t* W1q, const float* W1s, const int8_t* W3q,
+                   const float* W3s, const int8_t* W2q, const float* W2s, void* out, int T, int d, int dff, int E,
+                   int k, moe_stream_t stream) {
+  const W8Weights w8{W1q, W1s, W3q, W3s, W2q, W2s};
+  return forward_w8(x, Wg, w8, out, T, d, dff, E, k, nullptr, 0, true, stream);
 }
 
 int moe_get_device_status(moe_stream_t stream, int* status, int reset) {

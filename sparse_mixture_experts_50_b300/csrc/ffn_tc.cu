@@ -20,10 +20,27 @@
 // weights are never read.  The expert boundaries come from the device-side
 // offsets[E+1]; the host never reads the per-expert counts.
 //
+// int8 weights (KerasFormers Mixtral docs, "Lower memory": weight-only int8,
+// one fp32 scale per output row).  The weights stream from HBM as int8, half
+// the bytes of bf16, so the same kernel runs with:
+//   warp 0      TMA producer: per stage the bf16 A tile and the two raw int8
+//               B boxes (16 + 16 KB) into a 5-stage ring, so A is requested
+//               as early as the weights it meets;
+//   warps 6-9   converters: each widens its share of a stage's raw B to bf16
+//               (exact: every code in [-127, 127] is a bf16 value) and writes
+//               it into a 2-stage ring in the 128-byte-swizzled K-major
+//               layout tcgen05 reads;
+//   warp 1      MMA on A from the raw ring and B from the converted ring; a
+//               raw stage is free once the MMA and all converters are done;
+//   epilogue    multiplies each accumulator column by its row scale s[e, n]
+//               before the SwiGLU (gate/up) or the rounding (down): the scale
+//               of an output row factors out of its dot product.
+//
 // Every wait is bounded (globaltimer + iteration cap).  A wait that runs out
 // raises a CTA-wide abort flag and records MOE_ETIMEOUT; each role then
-// leaves its loop, the producer waits (bounded) for its copies in flight, the
-// MMA warp waits (bounded) for its MMAs, and TMEM is freed before returning.
+// leaves its loop, the TMA issuers wait (bounded) for their copies in
+// flight, the MMA warp waits (bounded) for its MMAs, and TMEM is freed
+// before returning.
 //
 // The set-up (barriers, tensor-map prefetch, TMEM allocation) runs before the
 // kernel waits on its predecessor (programmatic dependent launch), so it
@@ -38,23 +55,38 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;                  // rows (tokens) per tile
-constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row
+constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row of bf16
 constexpr int BN_HALF = 128;             // rows of one B box
 constexpr int BN = 2 * BN_HALF;          // MMA N
 constexpr int UMMA_K = 16;               // K of one tcgen05.mma (bf16)
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_HALF_BYTES = BN_HALF * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + 2 * B_HALF_BYTES;  // 48 KB
+constexpr int STAGE_BYTES = A_BYTES + 2 * B_HALF_BYTES;  // 48 KB: A + B in bf16
 constexpr int TMEM_COLS = 2 * BN;        // two fp32 accumulators
-constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
+#ifndef MOE_W8_CONV_WARPS
+#define MOE_W8_CONV_WARPS 4
+#endif
+#ifndef MOE_W8_STAGES
+#define MOE_W8_STAGES 5
+#endif
+#ifndef MOE_W8_CONV_STAGES
+#define MOE_W8_CONV_STAGES 2
+#endif
+constexpr int CONV_WARPS = MOE_W8_CONV_WARPS;  // int8 path: converter warps from warp 6
+constexpr int RAW_HALF_BYTES = BN_HALF * BK;          // one 128x64 int8 box, 8 KB
+constexpr int RAW_BYTES = 2 * RAW_HALF_BYTES;         // 16 KB per raw stage
+constexpr int MAX_STAGES = 6;
+constexpr int CONV_STAGES = MOE_W8_CONV_STAGES;  // int8 path: converted B stages (32 KB each)
+constexpr int CONV_BYTES = 2 * B_HALF_BYTES;
 constexpr int MAX_E = 64;
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 
 struct SmemCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];       // a stage's TMA copies landed
+  uint64_t empty[MAX_STAGES];      // the MMA (and, int8 path, every converter) is done with a stage
+  uint64_t c_full[CONV_STAGES];    // int8 path: converted B written
+  uint64_t c_empty[CONV_STAGES];   // int8 path: the MMA is done with converted B
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -65,11 +97,26 @@ struct SmemCtl {
   int seg[MAX_E + 1];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(SmemCtl);
+// Shared-memory plan of each weight format.  bf16: 4 stages of A + B.  int8:
+// 5 stages of A + raw B, then 2 stages of converted B.
+template <bool W8>
+struct Plan {
+  static constexpr int stages = W8 ? MOE_W8_STAGES : 4;
+  static constexpr int stage_bytes = W8 ? A_BYTES + RAW_BYTES : STAGE_BYTES;
+  static constexpr int conv_stages = W8 ? CONV_STAGES : 0;
+  static constexpr int threads = W8 ? 192 + 32 * CONV_WARPS : 192;
+  static constexpr size_t ring_bytes =
+      static_cast<size_t>(stages) * stage_bytes + static_cast<size_t>(conv_stages) * CONV_BYTES;
+  static constexpr size_t smem_bytes = 1024 + ring_bytes + sizeof(SmemCtl);
+};
+static_assert(Plan<true>::smem_bytes <= 227 * 1024, "int8 plan exceeds shared memory");
+static_assert(Plan<false>::smem_bytes <= 227 * 1024, "bf16 plan exceeds shared memory");
 
 struct GemmArgs {
   const int32_t* offsets;  // [E+1], device
   __nv_bfloat16* out;      // [Tk, ldo]
+  const float* scale0;     // int8 path: row scales of B0 [E * b_rows]
+  const float* scale1;     // int8 path: row scales of B1 (gate/up only)
   int ldo;                 // row stride of out (elements)
   int n_out;               // valid output columns
   int b_rows;              // rows per expert in the B tensor(s)
@@ -94,14 +141,13 @@ __device__ __forceinline__ void raise_abort(SmemCtl* ctl, int* status) {
   record_status(status, MOE_ETIMEOUT);
 }
 
-__device__ __forceinline__ void decode_tile(const SmemCtl* ctl, int E, int n_tiles, int tile, int& e, int& m, int& n) {
+__device__ __forceinline__ void decode_tile(const SmemCtl* ctl, int E, int tile, int& e, int& m, int& n) {
   e = 0;
   while (e + 1 < E && ctl->tile_prefix[e + 1] <= tile) ++e;
   const int local = tile - ctl->tile_prefix[e];
   const int mt = ctl->mtiles[e];
   n = local / mt;
   m = local - n * mt;
-  (void)n_tiles;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -109,13 +155,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <bool SWIGLU>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// Four int8 codes (one 32-bit word, element 0 in the low byte) -> four bf16
+// (two words), exactly.  Flipping the sign bit gives b + 128 in [0, 255] as an
+// unsigned byte; placed in the low mantissa bits of the fp32 2^23 it is the
+// fp32 value 2^23 + b + 128, and subtracting 2^23 + 128 leaves b exactly.  A
+// value of at most 8 significant bits has zero low 16 bits in fp32, so its
+// bf16 encoding is the high half of the fp32 word.
+__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  constexpr float kBias = 8388736.0f;  // 2^23 + 128
+  const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - kBias;
+  const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - kBias;
+  const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - kBias;
+  const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - kBias;
+  lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+  hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+}
+
+template <bool SWIGLU, bool W8>
+__global__ void __launch_bounds__(Plan<W8>::threads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+  constexpr int NST = Plan<W8>::stages;
+  constexpr int SB = Plan<W8>::stage_bytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* conv = smem + NST * SB;  // int8 path: converted B stages
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + Plan<W8>::ring_bytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const volatile int* abort_flag = &ctl->abort_flag;
@@ -123,9 +189,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // Set-up that reads nothing the previous kernel writes: barriers, tensor
   // maps, tensor memory.  It overlaps the previous kernel's tail.
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
-      ptx::mbar_init(&ctl->empty[s], 1);
+      ptx::mbar_init(&ctl->empty[s], W8 ? 1 + CONV_WARPS : 1);
+    }
+    for (int s = 0; s < Plan<W8>::conv_stages; ++s) {
+      ptx::mbar_init(&ctl->c_full[s], CONV_WARPS);
+      ptx::mbar_init(&ctl->c_empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ctl->tfull[a], 1);
@@ -178,15 +248,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
+      // bf16: A + both B boxes.  int8: A + both raw B boxes.
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t filled = 0;            // stages filled at least once
-      uint32_t last_parity[STAGES];   // parity of each stage's latest fill
-      for (int s = 0; s < STAGES; ++s) last_parity[s] = 0;
+      uint32_t filled = 0;                // stages filled at least once
+      uint32_t last_parity[MAX_STAGES];   // parity of each stage's latest fill
+      for (int s = 0; s < MAX_STAGES; ++s) last_parity[s] = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         int e, m, n;
-        decode_tile(ctl, args.E, args.n_tiles, tile, e, m, n);
+        decode_tile(ctl, args.E, tile, e, m, n);
         const int arow = ctl->seg[e] + m * BM;
         int b0row, b1row;
         if (SWIGLU) {
@@ -202,29 +273,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          uint8_t* sa = smem + stage * STAGE_BYTES;
-          ptx::mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
+          uint8_t* sa = smem + stage * SB;
+          constexpr int half = W8 ? RAW_HALF_BYTES : B_HALF_BYTES;
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage], SB);
           ptx::tma_load_2d(sa, &tmA, &ctl->full[stage], kb * BK, arow);
           ptx::tma_load_2d(sa + A_BYTES, &tmB0, &ctl->full[stage], kb * BK, b0row);
-          ptx::tma_load_2d(sa + A_BYTES + B_HALF_BYTES, SWIGLU ? &tmB1 : &tmB0, &ctl->full[stage], kb * BK, b1row);
+          ptx::tma_load_2d(sa + A_BYTES + half, SWIGLU ? &tmB1 : &tmB0, &ctl->full[stage], kb * BK, b1row);
           filled |= 1u << stage;
           last_parity[stage] = phase;
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       // No copy may still be writing shared memory when the CTA exits.
-      for (int s = 0; s < STAGES; ++s) {
+      for (int s = 0; s < NST; ++s) {
         if (filled & (1u << s)) ptx::mbar_wait(&ctl->full[s], last_parity[s], nullptr, drain_limit(args.wait_ns));
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, cstage = 0;
+      uint32_t phase = 0, cphase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -236,14 +308,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag, args.wait_ns)) {
+          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag, args.wait_ns) ||
+              (W8 && !ptx::mbar_wait(&ctl->c_full[cstage], cphase, abort_flag, args.wait_ns))) {
             raise_abort(ctl, args.status);
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sa = ptx::smem_u32(smem + stage * SB);
+          const uint32_t sb = W8 ? ptx::smem_u32(conv + cstage * CONV_BYTES) : sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             const uint64_t adesc = ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2);
@@ -251,7 +324,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::umma_bf16(d_tmem, adesc, bdesc, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           ptx::umma_commit(&ctl->empty[stage]);  // frees the stage once these MMAs are done
-          if (++stage == STAGES) {
+          if (W8) {
+            ptx::umma_commit(&ctl->c_empty[cstage]);
+            if (++cstage == CONV_STAGES) {
+              cstage = 0;
+              cphase ^= 1u;
+            }
+          }
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
@@ -267,7 +347,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::umma_commit(&ctl->drain);
       ptx::mbar_wait(&ctl->drain, 0, nullptr, drain_limit(args.wait_ns));
     }
-  } else {
+  } else if (warp < 6) {
     // -------------------------------------------------- epilogue (warps 2-5)
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. +31
     const int row_in_tile = quad * 32 + lane;
@@ -275,7 +355,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int e, m, n;
-      decode_tile(ctl, args.E, args.n_tiles, tile, e, m, n);
+      decode_tile(ctl, args.E, tile, e, m, n);
       const int grow = ctl->seg[e] + m * BM + row_in_tile;
       const bool row_ok = grow < ctl->seg[e + 1];
       // tcgen05.ld below is warp-collective: leave together or not at all.
@@ -295,11 +375,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tmem_ld_32x32b_x32(t_row + BN_HALF + c, u);
           ptx::tmem_ld_wait();
           if (row_ok && col0 + c < args.n_out) {
+            const size_t srow = static_cast<size_t>(e) * args.b_rows + col0 + c;
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+              float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+              if (W8) {
+                const float2 sg = __ldg(reinterpret_cast<const float2*>(args.scale0 + srow) + i);
+                const float2 su = __ldg(reinterpret_cast<const float2*>(args.scale1 + srow) + i);
+                g0 *= sg.x;
+                g1 *= sg.y;
+                u0 *= su.x;
+                u1 *= su.y;
+              }
               const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
               const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
               pk[i] = pack_bf16x2(h0, h1);
@@ -317,9 +406,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tmem_ld_32x32b_x32(t_row + c, v);
           ptx::tmem_ld_wait();
           if (row_ok && col0 + c < args.n_out) {
+            const size_t srow = static_cast<size_t>(e) * args.b_rows + col0 + c;
             uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            for (int i = 0; i < 16; ++i) {
+              float y0 = __uint_as_float(v[2 * i]), y1 = __uint_as_float(v[2 * i + 1]);
+              if (W8) {
+                const float2 sy = __ldg(reinterpret_cast<const float2*>(args.scale0 + srow) + i);
+                y0 *= sy.x;
+                y1 *= sy.y;
+              }
+              pk[i] = pack_bf16x2(y0, y1);
+            }
             uint4* dst = reinterpret_cast<uint4*>(args.out + static_cast<size_t>(grow) * args.ldo + col0 + c);
 #pragma unroll
             for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -331,6 +429,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+    }
+  } else if (W8) {
+    // -------------------------------------------------- converters (warps 6-9, int8 path)
+    // Per stage: wait until the MMA is done with the converted stage and the
+    // raw stage has landed, widen the raw B to bf16 into the swizzled layout,
+    // then mark the converted stage ready and release the raw stage.
+    const int ct = threadIdx.x - 192;  // 0 .. 32 * CONV_WARPS - 1
+    int stage = 0, cstage = 0;
+    uint32_t phase = 0, cphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < kblocks; ++kb) {
+        // Waits are warp-uniform: the warp goes on or leaves as one.
+        const bool ready = ptx::mbar_wait(&ctl->c_empty[cstage], cphase ^ 1u, abort_flag, args.wait_ns) &&
+                           ptx::mbar_wait(&ctl->full[stage], phase, abort_flag, args.wait_ns);
+        if (!__all_sync(0xFFFFFFFFu, ready)) {
+          raise_abort(ctl, args.status);
+          ok = false;
+          break;
+        }
+        // 1024 chunks of 16 codes: chunk ci is row ci/4 (of 256: B0 rows
+        // 0-127 then B1 rows), codes 16*(ci%4) .. +15 of the stage's 64.  A
+        // warp reads 512 consecutive bytes; its 16-byte stores land on
+        // distinct banks under the 128-byte swizzle (unit j of row r is
+        // stored at unit j ^ (r % 8)).
+        const uint32_t rs = ptx::smem_u32(smem + stage * SB + A_BYTES);
+        const uint32_t sb = ptx::smem_u32(conv + cstage * CONV_BYTES);
+        constexpr int kChunks = (RAW_BYTES / 16) / (32 * CONV_WARPS);
+        uint4 v[kChunks];
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) v[i] = ptx::lds128(rs + (i * (32 * CONV_WARPS) + ct) * 16);
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+          const int ci = i * (32 * CONV_WARPS) + ct;
+          const int r = ci >> 2;
+          const int kc = ci & 3;
+          uint4 lo, hi;
+          i8x4_to_bf16x4(v[i].x, lo.x, lo.y);
+          i8x4_to_bf16x4(v[i].y, lo.z, lo.w);
+          i8x4_to_bf16x4(v[i].z, hi.x, hi.y);
+          i8x4_to_bf16x4(v[i].w, hi.z, hi.w);
+          const uint32_t row = sb + r * 128;
+          const int sw = r & 7;
+          ptx::sts128(row + (((2 * kc) ^ sw) << 4), lo);
+          ptx::sts128(row + (((2 * kc + 1) ^ sw) << 4), hi);
+        }
+        ptx::fence_proxy_async_smem();  // the MMA reads these through the async proxy
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&ctl->c_full[cstage]);
+          ptx::mbar_arrive(&ctl->empty[stage]);
+        }
+        if (++cstage == CONV_STAGES) {
+          cstage = 0;
+          cphase ^= 1u;
+        }
+        if (++stage == NST) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   }
@@ -363,18 +522,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, inner] -> tensor map with 64 x 128 boxes,
-// 128-byte swizzle, zero fill outside the matrix.
-int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows) {
+// Row-major matrix [rows, inner] -> tensor map with 64 x 128 boxes and zero
+// fill outside the matrix.  bf16: 128-byte swizzle (the tcgen05 operand
+// layout).  int8: no swizzle (64-byte rows, read back by the converters).
+int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, bool int8) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return MOE_ECUDA;
+  const uint64_t esz = int8 ? 1 : 2;
   const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint64_t strides[1] = {inner * esz};
   const cuuint32_t box[2] = {BK, BN_HALF};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
 }
 
@@ -399,15 +561,15 @@ int balanced_grid(long long tiles, int num_sms) {
   return best;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool W8>
 int smem_attr_once(int device) {
   static std::mutex mu;
   static bool done[64] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return MOE_ECUDA;
   if (!done[device]) {
-    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(SMEM_BYTES)) != cudaSuccess) {
+    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, W8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Plan<W8>::smem_bytes)) != cudaSuccess) {
       return MOE_ECUDA;
     }
     done[device] = true;
@@ -415,26 +577,29 @@ int smem_attr_once(int device) {
   return MOE_OK;
 }
 
-template <bool SWIGLU>
-int launch_gemm(const void* A, const void* B0, const void* B1, const int32_t* offsets, void* out, int Tk, int K,
-                int n_out, int b_rows, int E, const Ctx& c, cudaStream_t s) {
+template <bool SWIGLU, bool W8>
+int launch_gemm(const void* A, const void* B0, const void* B1, const float* S0, const float* S1,
+                const int32_t* offsets, void* out, int Tk, int K, int n_out, int b_rows, int E, const Ctx& c,
+                cudaStream_t s) {
   if (Tk <= 0) return MOE_OK;
   CUtensorMap ta, tb0, tb1;
-  int rc = make_tmap(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(Tk));
+  int rc = make_tmap(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(Tk), false);
   if (rc != MOE_OK) return rc;
-  rc = make_tmap(&tb0, B0, static_cast<uint64_t>(K), static_cast<uint64_t>(E) * b_rows);
+  rc = make_tmap(&tb0, B0, static_cast<uint64_t>(K), static_cast<uint64_t>(E) * b_rows, W8);
   if (rc != MOE_OK) return rc;
   if (SWIGLU) {
-    rc = make_tmap(&tb1, B1, static_cast<uint64_t>(K), static_cast<uint64_t>(E) * b_rows);
+    rc = make_tmap(&tb1, B1, static_cast<uint64_t>(K), static_cast<uint64_t>(E) * b_rows, W8);
     if (rc != MOE_OK) return rc;
   } else {
     tb1 = tb0;
   }
-  rc = smem_attr_once<SWIGLU>(c.device);
+  rc = smem_attr_once<SWIGLU, W8>(c.device);
   if (rc != MOE_OK) return rc;
   GemmArgs a;
   a.offsets = offsets;
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.scale0 = S0;
+  a.scale1 = S1;
   a.ldo = n_out;
   a.n_out = n_out;
   a.b_rows = b_rows;
@@ -448,7 +613,7 @@ int launch_gemm(const void* A, const void* B0, const void* B1, const int32_t* of
   // per expert that has rows (at most min(E, Tk) of them).
   const long long max_tiles = (static_cast<long long>(Tk) / BM + (E < Tk ? E : Tk)) * a.n_tiles;
   const int grid = balanced_grid(max_tiles, c.num_sms);
-  launch_pdl(grouped_gemm_tc_kernel<SWIGLU>, grid, NUM_THREADS, SMEM_BYTES, s, ta, tb0, tb1, a);
+  launch_pdl(grouped_gemm_tc_kernel<SWIGLU, W8>, grid, Plan<W8>::threads, Plan<W8>::smem_bytes, s, ta, tb0, tb1, a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 
@@ -456,12 +621,23 @@ int launch_gemm(const void* A, const void* B0, const void* B1, const int32_t* of
 
 int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, void* h, int Tk,
                       int d, int dff, int E, const Ctx& c, cudaStream_t s) {
-  return launch_gemm<true>(x_perm, W1, W3, offsets, h, Tk, d, dff, dff, E, c, s);
+  return launch_gemm<true, false>(x_perm, W1, W3, nullptr, nullptr, offsets, h, Tk, d, dff, dff, E, c, s);
 }
 
 int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d, int dff, int E,
                    const Ctx& c, cudaStream_t s) {
-  return launch_gemm<false>(h, W2, nullptr, offsets, y, Tk, dff, d, d, E, c, s);
+  return launch_gemm<false, false>(h, W2, nullptr, nullptr, nullptr, offsets, y, Tk, dff, d, d, E, c, s);
+}
+
+int launch_w8_gate_up(const void* x_perm, const int32_t* offsets, const int8_t* W1q, const float* W1s,
+                      const int8_t* W3q, const float* W3s, void* h, int Tk, int d, int dff, int E, const Ctx& c,
+                      cudaStream_t s) {
+  return launch_gemm<true, true>(x_perm, W1q, W3q, W1s, W3s, offsets, h, Tk, d, dff, dff, E, c, s);
+}
+
+int launch_w8_down(const void* h, const int32_t* offsets, const int8_t* W2q, const float* W2s, void* y, int Tk, int d,
+                   int dff, int E, const Ctx& c, cudaStream_t s) {
+  return launch_gemm<false, true>(h, W2q, nullptr, W2s, nullptr, offsets, y, Tk, dff, d, d, E, c, s);
 }
 
 }  // namespace moe

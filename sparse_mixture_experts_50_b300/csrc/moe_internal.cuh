@@ -83,5 +83,13 @@ int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1
                       void* h, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d,
                    int dff, int E, const Ctx& c, cudaStream_t s);
+// int8 weight-only path: per-row int8 codes + fp32 scales, bf16 activations.
+cudaError_t launch_quantize_int8(const void* W, long long rows, int cols, int8_t* q, float* scale,
+                                 const Ctx& c, cudaStream_t s);
+int launch_w8_gate_up(const void* x_perm, const int32_t* offsets, const int8_t* W1q, const float* W1s,
+                      const int8_t* W3q, const float* W3s, void* h, int Tk, int d, int dff, int E,
+                      const Ctx& c, cudaStream_t s);
+int launch_w8_down(const void* h, const int32_t* offsets, const int8_t* W2q, const float* W2s, void* y,
+                   int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 
 }  // namespace moe
