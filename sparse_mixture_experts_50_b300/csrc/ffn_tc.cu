@@ -36,6 +36,19 @@
 //               before the SwiGLU (gate/up) or the rounding (down): the scale
 //               of an output row factors out of its dot product.
 //
+// Small batches (decode).  With a few tokens per expert a 128-row token tile
+// is mostly padding, and the per-stage token tile costs as much shared
+// memory as the weights.  So for small row counts the roles swap: a tile is
+// 256 weight rows x 32 tokens, computed as two M=128, N=32 MMAs per K step
+// (weights as the A operand, the token rows as B).  The accumulator lanes are
+// then weight rows: each epilogue thread owns one output column (one row
+// scale) for up to 32 tokens.  A stage is the 4 KB token tile + the weights,
+// so more stages fit and more weight bytes are in flight per SM.  With int8
+// weights the converters write the widened weight rows straight into tensor
+// memory (tcgen05.st, one row per lane, two bf16 per column) and the MMA
+// takes its A operand from there: the widened weights never touch shared
+// memory, whose bandwidth would otherwise bound the small-batch int8 GEMM.
+//
 // Every wait is bounded (globaltimer + iteration cap).  A wait that runs out
 // raises a CTA-wide abort flag and records MOE_ETIMEOUT; each role then
 // leaves its loop, the TMA issuers wait (bounded) for their copies in
@@ -55,14 +68,12 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;                  // rows (tokens) per tile
+constexpr int TN = 32;                   // swapped mode: tokens per tile (the MMA N)
 constexpr int BK = 64;                   // K per stage: one 128-byte swizzle row of bf16
 constexpr int BN_HALF = 128;             // rows of one B box
 constexpr int BN = 2 * BN_HALF;          // MMA N
 constexpr int UMMA_K = 16;               // K of one tcgen05.mma (bf16)
-constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_HALF_BYTES = BN_HALF * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + 2 * B_HALF_BYTES;  // 48 KB: A + B in bf16
-constexpr int TMEM_COLS = 2 * BN;        // two fp32 accumulators
 constexpr int EPI_THREADS = 128;
 #ifndef MOE_W8_CONV_WARPS
 #define MOE_W8_CONV_WARPS 4
@@ -73,20 +84,53 @@ constexpr int EPI_THREADS = 128;
 #ifndef MOE_W8_CONV_STAGES
 #define MOE_W8_CONV_STAGES 2
 #endif
+#ifndef MOE_SWAP_STAGES
+#define MOE_SWAP_STAGES 6
+#endif
+#ifndef MOE_W8_SWAP_STAGES
+#define MOE_W8_SWAP_STAGES 6
+#endif
+#ifndef MOE_CVT_F32X2
+#define MOE_CVT_F32X2 1
+#endif
+#ifndef MOE_TOK_STAGES
+#define MOE_TOK_STAGES 3
+#endif
+#ifndef MOE_TMEM_A_STAGES
+#define MOE_TMEM_A_STAGES 3
+#endif
+#ifndef MOE_SWAP_MAX_ROWS
+#define MOE_SWAP_MAX_ROWS 128
+#endif
 constexpr int CONV_WARPS = MOE_W8_CONV_WARPS;  // int8 path: converter warps from warp 6
 constexpr int RAW_HALF_BYTES = BN_HALF * BK;          // one 128x64 int8 box, 8 KB
 constexpr int RAW_BYTES = 2 * RAW_HALF_BYTES;         // 16 KB per raw stage
-constexpr int MAX_STAGES = 6;
+constexpr int MAX_STAGES = 10;
 constexpr int CONV_STAGES = MOE_W8_CONV_STAGES;  // int8 path: converted B stages (32 KB each)
 constexpr int CONV_BYTES = 2 * B_HALF_BYTES;
+// int8 small-batch mode: a stage covers 128 K of each weight row (128-byte
+// rows in every TMA request); its widened weights sit in tensor memory as two
+// 128-row halves x 128 K = 2 x 64 columns, after the 128 accumulator columns.
+constexpr int BK_W = 128;
+constexpr int RAW_W_HALF_BYTES = BN_HALF * BK_W;      // one 128x128 int8 box, 16 KB
+constexpr int TMEM_A_STAGES = MOE_TMEM_A_STAGES;
+constexpr int TMEM_A_COL0 = 128;
+constexpr int TMEM_A_HALF_COLS = BK_W / 2;
+constexpr int TMEM_A_STAGE_COLS = 2 * TMEM_A_HALF_COLS;
+constexpr int RING_MAX = CONV_STAGES > TMEM_A_STAGES ? CONV_STAGES : TMEM_A_STAGES;
 constexpr int MAX_E = 64;
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+constexpr uint32_t IDESC_SWAP = ptx::idesc_bf16_f32(BN_HALF, TN);
+// The swapped mode serves GEMMs of at most this many rows (tokens x k).
+constexpr int SWAP_MAX_ROWS = MOE_SWAP_MAX_ROWS;
 
 struct SmemCtl {
   uint64_t full[MAX_STAGES];       // a stage's TMA copies landed
   uint64_t empty[MAX_STAGES];      // the MMA (and, int8 path, every converter) is done with a stage
-  uint64_t c_full[CONV_STAGES];    // int8 path: converted B written
-  uint64_t c_empty[CONV_STAGES];   // int8 path: the MMA is done with converted B
+  uint64_t c_full[RING_MAX];       // int8 path: widened weights written (shared or tensor memory)
+  uint64_t c_empty[RING_MAX];      // int8 path: the MMA is done with widened weights
+  uint64_t tok_full[8];            // int8 small-batch mode: token tile landed
+  uint64_t tok_empty[8];           // int8 small-batch mode: the MMA is done with a token tile
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -97,20 +141,44 @@ struct SmemCtl {
   int seg[MAX_E + 1];
 };
 
-// Shared-memory plan of each weight format.  bf16: 4 stages of A + B.  int8:
-// 5 stages of A + raw B, then 2 stages of converted B.
-template <bool W8>
+// Plan of each mode.  A shared-memory stage is the token tile (128 rows, or
+// 32 when swapped) + the weights (bf16, or raw int8).  bf16: 4 stages (6
+// swapped).  int8: 5 stages + 2 stages of widened weights in shared memory.
+// int8 swapped: the weights no longer wait for the MMA (it reads them from
+// tensor memory), so they get a ring of their own, 6 stages of 256 rows x
+// 128 K, freed by the converters; the token tiles have a 3-stage ring with
+// a producer warp of their own, freed by the MMA; 3 stages of widened
+// weights in tensor memory.
+template <bool W8, bool SWAP>
 struct Plan {
-  static constexpr int stages = W8 ? MOE_W8_STAGES : 4;
-  static constexpr int stage_bytes = W8 ? A_BYTES + RAW_BYTES : STAGE_BYTES;
-  static constexpr int conv_stages = W8 ? CONV_STAGES : 0;
-  static constexpr int threads = W8 ? 192 + 32 * CONV_WARPS : 192;
-  static constexpr size_t ring_bytes =
-      static_cast<size_t>(stages) * stage_bytes + static_cast<size_t>(conv_stages) * CONV_BYTES;
+  static constexpr bool tmem_a = W8 && SWAP;             // A operand (widened weights) in tensor memory
+  static constexpr int kstep = tmem_a ? BK_W : BK;       // K per stage
+  static constexpr int rows = SWAP ? TN : BM;            // token rows per tile
+  static constexpr int tok_box_bytes = rows * BK * 2;    // one 64-wide token box
+  static constexpr int a_bytes = (kstep / BK) * tok_box_bytes;  // token tile per stage
+  static constexpr int raw_half_bytes = tmem_a ? RAW_W_HALF_BYTES : RAW_HALF_BYTES;
+  static constexpr int b_off = tmem_a ? 0 : a_bytes;     // weights' offset in a stage
+  static constexpr int stage_bytes = b_off + (W8 ? 2 * raw_half_bytes : 2 * B_HALF_BYTES);
+  static constexpr int tok_stages = tmem_a ? MOE_TOK_STAGES : 0;  // separate token ring
+  static constexpr int tok_warp = 6 + CONV_WARPS;        // its producer (int8 swapped)
+  static constexpr int stages = SWAP ? (W8 ? MOE_W8_SWAP_STAGES : MOE_SWAP_STAGES) : (W8 ? MOE_W8_STAGES : 4);
+  static constexpr int conv_stages = (W8 && !SWAP) ? CONV_STAGES : 0;  // shared-memory widened stages
+  static constexpr int wide_stages = tmem_a ? TMEM_A_STAGES : CONV_STAGES;
+  static constexpr int threads = W8 ? 192 + 32 * CONV_WARPS + (tmem_a ? 32 : 0) : 192;
+  static constexpr int acc_cols = SWAP ? 2 * TN : BN;    // fp32 columns of one accumulator
+  static constexpr int tmem_cols = (SWAP && !W8) ? 128 : 512;  // power of two
+  static_assert(!tmem_a || TMEM_A_COL0 + TMEM_A_STAGES * TMEM_A_STAGE_COLS <= 512, "tensor-memory ring too deep");
+  static_assert(!tmem_a || 2 * acc_cols <= TMEM_A_COL0, "accumulators overlap the widened weights");
+  static_assert(!tmem_a || CONV_WARPS == 4 || CONV_WARPS == 8, "converter warps per tensor-memory lane quarter: 1 or 2");
+  static_assert(tok_stages <= 8, "token ring too deep");
+  static constexpr size_t ring_bytes = static_cast<size_t>(stages) * stage_bytes +
+                                       static_cast<size_t>(conv_stages) * CONV_BYTES +
+                                       static_cast<size_t>(tok_stages) * a_bytes;
   static constexpr size_t smem_bytes = 1024 + ring_bytes + sizeof(SmemCtl);
+  static_assert(stages <= MAX_STAGES, "too many stages");
+  static_assert(smem_bytes <= 227 * 1024, "plan exceeds shared memory");
+  static_assert(2 * acc_cols <= tmem_cols, "accumulators exceed the tensor-memory allocation");
 };
-static_assert(Plan<true>::smem_bytes <= 227 * 1024, "int8 plan exceeds shared memory");
-static_assert(Plan<false>::smem_bytes <= 227 * 1024, "bf16 plan exceeds shared memory");
 
 struct GemmArgs {
   const int32_t* offsets;  // [E+1], device
@@ -163,6 +231,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // bf16 encoding is the high half of the fp32 word.
 __device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;
+#if MOE_CVT_F32X2
+  // The two subtractions of a pair as one packed fp32x2 add of -(2^23 + 128).
+  constexpr unsigned long long kBias2 = 0xCB000080CB000080ull;
+  unsigned long long p01 = (static_cast<unsigned long long>(__byte_perm(u, 0x4B000000u, 0x7541)) << 32) |
+                           __byte_perm(u, 0x4B000000u, 0x7540);
+  unsigned long long p23 = (static_cast<unsigned long long>(__byte_perm(u, 0x4B000000u, 0x7543)) << 32) |
+                           __byte_perm(u, 0x4B000000u, 0x7542);
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p01) : "l"(kBias2));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p23) : "l"(kBias2));
+  lo = __byte_perm(static_cast<uint32_t>(p01), static_cast<uint32_t>(p01 >> 32), 0x7632);
+  hi = __byte_perm(static_cast<uint32_t>(p23), static_cast<uint32_t>(p23 >> 32), 0x7632);
+#else
   constexpr float kBias = 8388736.0f;  // 2^23 + 128
   const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - kBias;
   const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - kBias;
@@ -170,18 +250,23 @@ __device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_
   const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - kBias;
   lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
   hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+#endif
 }
 
-template <bool SWIGLU, bool W8>
-__global__ void __launch_bounds__(Plan<W8>::threads, 1)
+template <bool SWIGLU, bool W8, bool SWAP>
+__global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
-  constexpr int NST = Plan<W8>::stages;
-  constexpr int SB = Plan<W8>::stage_bytes;
+  using P = Plan<W8, SWAP>;
+  constexpr int NST = P::stages;
+  constexpr int SB = P::stage_bytes;
+  constexpr int AB = P::a_bytes;
+  constexpr int ROWS = P::rows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* conv = smem + NST * SB;  // int8 path: converted B stages
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + Plan<W8>::ring_bytes);
+  uint8_t* toks = smem + NST * SB;  // int8 swapped: token ring (no converted stages then)
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + P::ring_bytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const volatile int* abort_flag = &ctl->abort_flag;
@@ -191,9 +276,13 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
-      ptx::mbar_init(&ctl->empty[s], W8 ? 1 + CONV_WARPS : 1);
+      ptx::mbar_init(&ctl->empty[s], W8 ? (P::tmem_a ? 0 : 1) + CONV_WARPS : 1);
     }
-    for (int s = 0; s < Plan<W8>::conv_stages; ++s) {
+    for (int s = 0; s < P::tok_stages; ++s) {
+      ptx::mbar_init(&ctl->tok_full[s], 1);
+      ptx::mbar_init(&ctl->tok_empty[s], 1);
+    }
+    for (int s = 0; s < (W8 ? P::wide_stages : 0); ++s) {
       ptx::mbar_init(&ctl->c_full[s], CONV_WARPS);
       ptx::mbar_init(&ctl->c_empty[s], 1);
     }
@@ -211,7 +300,7 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
     if (SWIGLU) ptx::prefetch_tmap(&tmB1);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    ptx::tmem_alloc(&ctl->tmem_base, P::tmem_cols);
     ptx::tmem_relinquish();
   }
   pdl_enter();
@@ -232,7 +321,7 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
     }
     for (int e = 0; e < args.E; ++e) {
       const int n_e = ctl->seg[e + 1] - ctl->seg[e];
-      const int mt = (n_e + BM - 1) / BM;
+      const int mt = (n_e + ROWS - 1) / ROWS;
       ctl->mtiles[e] = mt;
       run += mt * args.n_tiles;
       ctl->tile_prefix[e + 1] = run;
@@ -243,7 +332,7 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   const int total_tiles = ctl->tile_prefix[args.E];
-  const int kblocks = (args.K + BK - 1) / BK;
+  const int kblocks = (args.K + P::kstep - 1) / P::kstep;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -258,7 +347,7 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         int e, m, n;
         decode_tile(ctl, args.E, tile, e, m, n);
-        const int arow = ctl->seg[e] + m * BM;
+        const int arow = ctl->seg[e] + m * ROWS;
         int b0row, b1row;
         if (SWIGLU) {
           b0row = e * args.b_rows + n * BN_HALF;
@@ -274,11 +363,16 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
             break;
           }
           uint8_t* sa = smem + stage * SB;
-          constexpr int half = W8 ? RAW_HALF_BYTES : B_HALF_BYTES;
+          constexpr int half = W8 ? P::raw_half_bytes : B_HALF_BYTES;
+          const int k0 = kb * P::kstep;
           ptx::mbar_arrive_expect_tx(&ctl->full[stage], SB);
-          ptx::tma_load_2d(sa, &tmA, &ctl->full[stage], kb * BK, arow);
-          ptx::tma_load_2d(sa + A_BYTES, &tmB0, &ctl->full[stage], kb * BK, b0row);
-          ptx::tma_load_2d(sa + A_BYTES + half, SWIGLU ? &tmB1 : &tmB0, &ctl->full[stage], kb * BK, b1row);
+          if (!P::tmem_a) {
+#pragma unroll
+            for (int t = 0; t < P::kstep / BK; ++t)
+              ptx::tma_load_2d(sa + t * P::tok_box_bytes, &tmA, &ctl->full[stage], k0 + t * BK, arow);
+          }
+          ptx::tma_load_2d(sa + P::b_off, &tmB0, &ctl->full[stage], k0, b0row);
+          ptx::tma_load_2d(sa + P::b_off + half, SWIGLU ? &tmB1 : &tmB0, &ctl->full[stage], k0, b1row);
           filled |= 1u << stage;
           last_parity[stage] = phase;
           if (++stage == NST) {
@@ -306,32 +400,53 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * P::acc_cols);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag, args.wait_ns) ||
+          // int8 swapped: the token ring (the weights arrive via c_full);
+          // otherwise the operand stage.
+          if (!ptx::mbar_wait(P::tmem_a ? &ctl->tok_full[stage] : &ctl->full[stage], phase, abort_flag,
+                              args.wait_ns) ||
               (W8 && !ptx::mbar_wait(&ctl->c_full[cstage], cphase, abort_flag, args.wait_ns))) {
             raise_abort(ctl, args.status);
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(smem + stage * SB);
-          const uint32_t sb = W8 ? ptx::smem_u32(conv + cstage * CONV_BYTES) : sa + A_BYTES;
+          const uint32_t sa = P::tmem_a ? ptx::smem_u32(toks + stage * AB) : ptx::smem_u32(smem + stage * SB);
+          const uint32_t sb = (W8 && !SWAP) ? ptx::smem_u32(conv + cstage * CONV_BYTES) : sa + AB;
+          const uint32_t ta = tmem_base + TMEM_A_COL0 + static_cast<uint32_t>(cstage * TMEM_A_STAGE_COLS);
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t adesc = ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2);
-            const uint64_t bdesc = ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2);
-            ptx::umma_bf16(d_tmem, adesc, bdesc, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < P::kstep / UMMA_K; ++kk) {
+            const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
+            // token operand: 64-wide box kk / 4, K offset (kk % 4) * 16 within it
+            const uint64_t tdesc = ptx::sdesc_kmajor_sw128(sa + (kk / (BK / UMMA_K)) * P::tok_box_bytes +
+                                                           (kk % (BK / UMMA_K)) * UMMA_K * 2);
+            if (P::tmem_a) {
+              // widened weights (two 128-lane halves in tensor memory) x the 32-token tile
+              ptx::umma_bf16_tmem_a(d_tmem, ta + kk * (UMMA_K / 2), tdesc, IDESC_SWAP, acc_flag);
+              ptx::umma_bf16_tmem_a(d_tmem + TN, ta + TMEM_A_HALF_COLS + kk * (UMMA_K / 2), tdesc, IDESC_SWAP,
+                                    acc_flag);
+            } else if (SWAP) {
+              // weights (two 128-row halves) x the 32-token tile
+              const uint64_t w0 = ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2);
+              const uint64_t w1 = ptx::sdesc_kmajor_sw128(sb + B_HALF_BYTES + kk * UMMA_K * 2);
+              ptx::umma_bf16(d_tmem, w0, tdesc, IDESC_SWAP, acc_flag);
+              ptx::umma_bf16(d_tmem + TN, w1, tdesc, IDESC_SWAP, acc_flag);
+            } else {
+              const uint64_t bdesc = ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2);
+              ptx::umma_bf16(d_tmem, tdesc, bdesc, IDESC, acc_flag);
+            }
           }
-          ptx::umma_commit(&ctl->empty[stage]);  // frees the stage once these MMAs are done
+          // frees the stage (int8 swapped: the token stage) once these MMAs are done
+          ptx::umma_commit(P::tmem_a ? &ctl->tok_empty[stage] : &ctl->empty[stage]);
           if (W8) {
             ptx::umma_commit(&ctl->c_empty[cstage]);
-            if (++cstage == CONV_STAGES) {
+            if (++cstage == P::wide_stages) {
               cstage = 0;
               cphase ^= 1u;
             }
           }
-          if (++stage == NST) {
+          if (++stage == (P::tmem_a ? P::tok_stages : NST)) {
             stage = 0;
             phase ^= 1u;
           }
@@ -356,7 +471,7 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int e, m, n;
       decode_tile(ctl, args.E, tile, e, m, n);
-      const int grow = ctl->seg[e] + m * BM + row_in_tile;
+      const int grow = ctl->seg[e] + m * ROWS + row_in_tile;
       const bool row_ok = grow < ctl->seg[e + 1];
       // tcgen05.ld below is warp-collective: leave together or not at all.
       const bool ready = ptx::mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag, args.wait_ns);
@@ -365,8 +480,35 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if (SWIGLU) {
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * P::acc_cols);
+      if (SWAP) {
+        // Lane = weight row within a 128-row half; columns = the tile's tokens.
+        const int row0 = ctl->seg[e] + m * TN;
+        const int rows_here = min(TN, ctl->seg[e + 1] - row0);
+#pragma unroll 1
+        for (int hf = 0; hf < (SWIGLU ? 1 : 2); ++hf) {
+          uint32_t a[32], b[32];
+          ptx::tmem_ld_32x32b_x32(t_row + hf * TN, a);
+          if (SWIGLU) ptx::tmem_ld_32x32b_x32(t_row + TN, b);
+          ptx::tmem_ld_wait();
+          const int col = SWIGLU ? n * BN_HALF + row_in_tile : n * BN + hf * BN_HALF + row_in_tile;
+          if (col < args.n_out) {
+            const size_t srow = static_cast<size_t>(e) * args.b_rows + col;
+            const float s0 = W8 ? __ldg(args.scale0 + srow) : 1.0f;
+            const float s1 = (W8 && SWIGLU) ? __ldg(args.scale1 + srow) : 1.0f;
+            __nv_bfloat16* dst = args.out + static_cast<size_t>(row0) * args.ldo + col;
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+              if (j < rows_here) {
+                float v = s0 * __uint_as_float(a[j]);
+                if (SWIGLU) v = v / (1.0f + __expf(-v)) * (s1 * __uint_as_float(b[j]));
+                dst[static_cast<size_t>(j) * args.ldo] = __float2bfloat16_rn(v);
+              }
+            }
+          }
+        }
+      } else if (SWIGLU) {
         const int col0 = n * BN_HALF;
 #pragma unroll 1
         for (int c = 0; c < BN_HALF; c += 32) {
@@ -431,6 +573,41 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
         acc_phase ^= 1u;
       }
     }
+  } else if (P::tmem_a && warp == P::tok_warp) {
+    if (lane == 0) {
+      // ------------------------------------------------ token-tile producer (int8 swapped)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0;
+      uint32_t last_parity[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        int e, m, n;
+        decode_tile(ctl, args.E, tile, e, m, n);
+        const int arow = ctl->seg[e] + m * ROWS;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait(&ctl->tok_empty[stage], phase ^ 1u, abort_flag, args.wait_ns)) {
+            raise_abort(ctl, args.status);
+            ok = false;
+            break;
+          }
+          uint8_t* st = toks + stage * AB;
+          ptx::mbar_arrive_expect_tx(&ctl->tok_full[stage], AB);
+#pragma unroll
+          for (int t = 0; t < P::kstep / BK; ++t)
+            ptx::tma_load_2d(st + t * P::tok_box_bytes, &tmA, &ctl->tok_full[stage], kb * P::kstep + t * BK, arow);
+          filled |= 1u << stage;
+          last_parity[stage] = phase;
+          if (++stage == P::tok_stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < P::tok_stages; ++s) {
+        if (filled & (1u << s)) ptx::mbar_wait(&ctl->tok_full[s], last_parity[s], nullptr, drain_limit(args.wait_ns));
+      }
+    }
   } else if (W8) {
     // -------------------------------------------------- converters (warps 6-9, int8 path)
     // Per stage: wait until the MMA is done with the converted stage and the
@@ -450,12 +627,62 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
           ok = false;
           break;
         }
+        if (P::tmem_a) {
+          // Warp q (= warp % 4) may access tensor-memory lanes 32q .. 32q+31:
+          // lane r holds weight row r of a 128-row half, 128 K values as 64
+          // columns.  With 4 converter warps each does both halves; with 8,
+          // warps 6-9 do half 0 and warps 10-13 half 1.  The raw tile was
+          // stored with the 128-byte swizzle (16-byte unit u of row r at unit
+          // u ^ (r % 8)), so the row reads of 8 lanes hit distinct banks.
+          const int r = (warp & 3) * 32 + lane;
+          const uint32_t rs = ptx::smem_u32(smem + stage * SB + P::b_off) + r * BK_W;
+          const uint32_t tl = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + TMEM_A_COL0 +
+                              static_cast<uint32_t>(cstage * TMEM_A_STAGE_COLS);
+          constexpr int kHalves = CONV_WARPS == 8 ? 1 : 2;
+          const int hf0 = CONV_WARPS == 8 ? (warp - 6) / 4 : 0;
+#pragma unroll
+          for (int hi = 0; hi < kHalves; ++hi) {
+            const int hf = hf0 + hi;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {  // 64 codes = 32 columns at a time
+              uint4 v[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                v[u] = ptx::lds128(rs + hf * RAW_W_HALF_BYTES + (((4 * q + u) ^ (r & 7)) << 4));
+              uint32_t w[32];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                i8x4_to_bf16x4(v[u].x, w[8 * u + 0], w[8 * u + 1]);
+                i8x4_to_bf16x4(v[u].y, w[8 * u + 2], w[8 * u + 3]);
+                i8x4_to_bf16x4(v[u].z, w[8 * u + 4], w[8 * u + 5]);
+                i8x4_to_bf16x4(v[u].w, w[8 * u + 6], w[8 * u + 7]);
+              }
+              ptx::tmem_st_32x32b_x32(tl + hf * TMEM_A_HALF_COLS + q * 32, w);
+            }
+          }
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive(&ctl->c_full[cstage]);
+            ptx::mbar_arrive(&ctl->empty[stage]);
+          }
+          if (++cstage == P::wide_stages) {
+            cstage = 0;
+            cphase ^= 1u;
+          }
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         // 1024 chunks of 16 codes: chunk ci is row ci/4 (of 256: B0 rows
         // 0-127 then B1 rows), codes 16*(ci%4) .. +15 of the stage's 64.  A
         // warp reads 512 consecutive bytes; its 16-byte stores land on
         // distinct banks under the 128-byte swizzle (unit j of row r is
         // stored at unit j ^ (r % 8)).
-        const uint32_t rs = ptx::smem_u32(smem + stage * SB + A_BYTES);
+        const uint32_t rs = ptx::smem_u32(smem + stage * SB + AB);
         const uint32_t sb = ptx::smem_u32(conv + cstage * CONV_BYTES);
         constexpr int kChunks = (RAW_BYTES / 16) / (32 * CONV_WARPS);
         uint4 v[kChunks];
@@ -482,7 +709,7 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
           ptx::mbar_arrive(&ctl->c_full[cstage]);
           ptx::mbar_arrive(&ctl->empty[stage]);
         }
-        if (++cstage == CONV_STAGES) {
+        if (++cstage == P::wide_stages) {
           cstage = 0;
           cphase ^= 1u;
         }
@@ -499,7 +726,7 @@ __global__ void __launch_bounds__(Plan<W8>::threads, 1)
   ptx::tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    ptx::tmem_dealloc(tmem_base, P::tmem_cols);
   }
 }
 
@@ -522,20 +749,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major matrix [rows, inner] -> tensor map with 64 x 128 boxes and zero
-// fill outside the matrix.  bf16: 128-byte swizzle (the tcgen05 operand
-// layout).  int8: no swizzle (64-byte rows, read back by the converters).
-int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, bool int8) {
+// Row-major matrix [rows, inner] -> tensor map with 64 x box_rows boxes (128 x
+// box_rows for wide int8) and zero fill outside the matrix.  bf16: 128-byte
+// swizzle (the tcgen05 operand layout).  int8: 64-byte rows, unswizzled (read
+// back 16 bytes per thread along rows), or 128-byte rows with the 128-byte
+// swizzle (read back one row per thread).
+int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, bool int8, int box_rows,
+              bool wide_int8 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return MOE_ECUDA;
   const uint64_t esz = int8 ? 1 : 2;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner * esz};
-  const cuuint32_t box[2] = {BK, BN_HALF};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(wide_int8 ? BK_W : BK), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                        (int8 && !wide_int8) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
 }
@@ -561,15 +791,15 @@ int balanced_grid(long long tiles, int num_sms) {
   return best;
 }
 
-template <bool SWIGLU, bool W8>
+template <bool SWIGLU, bool W8, bool SWAP>
 int smem_attr_once(int device) {
   static std::mutex mu;
   static bool done[64] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return MOE_ECUDA;
   if (!done[device]) {
-    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, W8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Plan<W8>::smem_bytes)) != cudaSuccess) {
+    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, W8, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Plan<W8, SWAP>::smem_bytes)) != cudaSuccess) {
       return MOE_ECUDA;
     }
     done[device] = true;
@@ -577,24 +807,37 @@ int smem_attr_once(int device) {
   return MOE_OK;
 }
 
+template <bool SWIGLU, bool W8, bool SWAP>
+int launch_mode(const void* A, const void* B0, const void* B1, GemmArgs a, const Ctx& c, cudaStream_t s) {
+  using P = Plan<W8, SWAP>;
+  CUtensorMap ta, tb0, tb1;
+  int rc = make_tmap(&ta, A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.Tk), false, P::rows);
+  if (rc != MOE_OK) return rc;
+  const uint64_t brows = static_cast<uint64_t>(a.E) * a.b_rows;
+  rc = make_tmap(&tb0, B0, static_cast<uint64_t>(a.K), brows, W8, BN_HALF, P::tmem_a);
+  if (rc != MOE_OK) return rc;
+  if (SWIGLU) {
+    rc = make_tmap(&tb1, B1, static_cast<uint64_t>(a.K), brows, W8, BN_HALF, P::tmem_a);
+    if (rc != MOE_OK) return rc;
+  } else {
+    tb1 = tb0;
+  }
+  rc = smem_attr_once<SWIGLU, W8, SWAP>(c.device);
+  if (rc != MOE_OK) return rc;
+  // Upper bound on tiles: whole row blocks plus at most one partial block
+  // per expert that has rows (at most min(E, Tk) of them).
+  const long long max_tiles =
+      (static_cast<long long>(a.Tk) / P::rows + (a.E < a.Tk ? a.E : a.Tk)) * static_cast<long long>(a.n_tiles);
+  const int grid = balanced_grid(max_tiles, c.num_sms);
+  launch_pdl(grouped_gemm_tc_kernel<SWIGLU, W8, SWAP>, grid, P::threads, P::smem_bytes, s, ta, tb0, tb1, a);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
+
 template <bool SWIGLU, bool W8>
 int launch_gemm(const void* A, const void* B0, const void* B1, const float* S0, const float* S1,
                 const int32_t* offsets, void* out, int Tk, int K, int n_out, int b_rows, int E, const Ctx& c,
                 cudaStream_t s) {
   if (Tk <= 0) return MOE_OK;
-  CUtensorMap ta, tb0, tb1;
-  int rc = make_tmap(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(Tk), false);
-  if (rc != MOE_OK) return rc;
-  rc = make_tmap(&tb0, B0, static_cast<uint64_t>(K), static_cast<uint64_t>(E) * b_rows, W8);
-  if (rc != MOE_OK) return rc;
-  if (SWIGLU) {
-    rc = make_tmap(&tb1, B1, static_cast<uint64_t>(K), static_cast<uint64_t>(E) * b_rows, W8);
-    if (rc != MOE_OK) return rc;
-  } else {
-    tb1 = tb0;
-  }
-  rc = smem_attr_once<SWIGLU, W8>(c.device);
-  if (rc != MOE_OK) return rc;
   GemmArgs a;
   a.offsets = offsets;
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -609,12 +852,9 @@ int launch_gemm(const void* A, const void* B0, const void* B1, const float* S0, 
   a.n_tiles = SWIGLU ? (n_out + BN_HALF - 1) / BN_HALF : (n_out + BN - 1) / BN;
   a.status = c.status;
   a.wait_ns = c.wait_ns;
-  // Upper bound on tiles: whole row blocks plus at most one partial block
-  // per expert that has rows (at most min(E, Tk) of them).
-  const long long max_tiles = (static_cast<long long>(Tk) / BM + (E < Tk ? E : Tk)) * a.n_tiles;
-  const int grid = balanced_grid(max_tiles, c.num_sms);
-  launch_pdl(grouped_gemm_tc_kernel<SWIGLU, W8>, grid, Plan<W8>::threads, Plan<W8>::smem_bytes, s, ta, tb0, tb1, a);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
+  // Few rows (decode): weights as the MMA's M operand, 32 tokens as N.
+  if (Tk <= SWAP_MAX_ROWS) return launch_mode<SWIGLU, W8, true>(A, B0, B1, a, c, s);
+  return launch_mode<SWIGLU, W8, false>(A, B0, B1, a, c, s);
 }
 
 }  // namespace

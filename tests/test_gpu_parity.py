@@ -182,6 +182,8 @@ def test_expert_gate_up_and_down(B, name):
     [1000, 0, 0, 0, 0, 0, 0, 0],          # every row in one expert
     [0, 0, 0, 0, 0, 0, 0, 7],             # only the last expert
     [3, 1, 4, 1, 5, 9, 2, 6],             # decode-like: a few rows each
+    [40, 0, 33, 1, 32, 0, 22, 0],         # 128 rows: small-batch tiles of 32 tokens, ragged
+    [0, 0, 0, 128, 0, 0, 0, 0],           # 128 rows in one expert: four 32-token tiles
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_expert_tiles(B, counts, dtype):

@@ -92,6 +92,8 @@ def test_quantize_bit_exact(B, shape):
     [0, 128, 129, 1, 0, 255, 256, 300],  # tile boundaries, empty experts
     [1000, 0, 0, 0, 0, 0, 0, 0],          # every row in one expert
     [3, 1, 4, 1, 5, 9, 2, 6],             # decode-like: a few rows each
+    [40, 0, 33, 1, 32, 0, 22, 0],         # 128 rows: small-batch tiles of 32 tokens, ragged
+    [0, 0, 0, 128, 0, 0, 0, 0],           # 128 rows in one expert: four 32-token tiles
 ])
 def test_expert_w8_tiles(B, counts):
     """The int8 grouped GEMMs on hand-made segments; d and d_ff are not
