@@ -94,9 +94,10 @@ def kernel_source_hash():
 
 
 def ncu_traffic(workload):
-    """DRAM bytes per gate/up launch from a committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"gate_up_{workload}.md")
+    """DRAM bytes (read + write) per gate/up launch from the committed ncu
+    summary profiles/gemm_<workload>.md, if it was taken on the current
+    kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"gemm_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
