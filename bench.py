@@ -299,6 +299,7 @@ def bench_workload(name, shared, args, device, peaks, dist_on):
         "kernel_ms": {p: sum(v) / len(v) for p, v in parts.items()},
         "expert_counts": counts,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     **({"frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]} if bound == "tensor" else {}),
                      "kernel": "grouped_gemm_tc_kernel<gate_up+SwiGLU%s>" % (", int8 weights" if wl.w8 else ""),
                      "algorithmic_per_launch": gu_bytes if bound == "hbm" else gu_flops,
                      "traffic": ncu_traffic(name)},
@@ -452,15 +453,16 @@ def main():
     ensure_built()
     peaks = load_peaks()
     shared = {}
-    clocks = ClockSampler(local)
     results = {}
     head_layer = None
     for name in names:
-        if name == head_name:
-            clocks.start()
+        # SM clocks are sampled during every workload: the dense ones run at
+        # the power cap, below the maximum clock.
+        clocks = ClockSampler(local)
+        clocks.start()
         res, layer = bench_workload(name, shared, args, device, peaks, dist_on)
+        res["clocks"] = clocks.stop()
         if name == head_name:
-            res["clocks"] = clocks.stop()
             head_layer = layer
         else:
             del layer
@@ -493,7 +495,8 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": KERNELS_PER_STEP[mw.get(head_name).block] * args.steps,
             "clocks": head.get("clocks"),
-            "workloads": {n: {k: v for k, v in r.items() if k not in ("clocks",)} for n, r in results.items()},
+            "workloads": {n: {**{k: v for k, v in r.items() if k != "clocks"},
+                              "sm_mhz": (r.get("clocks") or {}).get("sm_mhz")} for n, r in results.items()},
         }
         print(json.dumps(line), flush=True)
     if dist_on:
