@@ -255,3 +255,63 @@ def moe_forward_w8(x, Wg, q1, s1, q3, s3, q2, s2, k):
     W3 = dequantize_int8_rows(q3, s3)
     W2 = dequantize_int8_rows(q2, s2)
     return moe_forward(x, Wg, W1, W3, W2, k)
+
+
+# ---------------------------------------------------------------- backward
+# Mixtral 8x7B model reference page, Training: the experts and the router are
+# trained together, so the layer is differentiated with respect to its input,
+# the gate and every expert matrix.  The top-k choice is piecewise constant in
+# the logits, so gradients flow through the k chosen logits only (through the
+# softmax over them) and through the chosen experts.
+def silu_grad(a) -> np.ndarray:
+    """d/da [a * sigmoid(a)] = sigmoid(a) * (1 + a * (1 - sigmoid(a)))."""
+    s = 1.0 / (1.0 + np.exp(-a))
+    return s * (1.0 + a * (1.0 - s))
+
+
+def moe_backward(x, Wg, W1, W3, W2, k, dout):
+    """Gradients of L = sum(out * dout) for out = moe_forward(x, ...).
+
+    Returns dict(dx[T,d], dWg[E,d], dW1[E,F,d], dW3[E,F,d], dW2[E,d,F]) in fp64,
+    following the chain rule step by step:
+      dy_j = w_j dout             (each chosen expert's output gradient)
+      dw_j = <dout, y_j>          (gate weight gradient)
+      dl_j = w_j (dw_j - sum_i w_i dw_i)   (softmax over the k chosen logits)
+      dh   = dy W2_e,  da = dh * b * silu'(a),  db = dh * silu(a)
+      dx  += da W1_e + db W3_e + sum_j dl_j Wg[i_j]
+      dW2_e += dy^T h,  dW1_e += da^T x,  dW3_e += db^T x,  dWg[i_j] += dl_j x
+    """
+    x = f64(x)
+    dout = f64(dout)
+    W1, W3, W2, Wg = f64(W1), f64(W3), f64(W2), f64(Wg)
+    T, d = x.shape
+    E = W1.shape[0]
+    w, idx, _ = router(x, Wg, k)
+    dx = np.zeros_like(x)
+    dWg = np.zeros_like(Wg)
+    dW1, dW3, dW2 = np.zeros_like(W1), np.zeros_like(W3), np.zeros_like(W2)
+    dw = np.zeros((T, k))
+    for j in range(k):
+        for e in range(E):
+            rows = np.nonzero(idx[:, j] == e)[0]
+            if rows.size == 0:
+                continue
+            xe = x[rows]
+            a = xe @ W1[e].T
+            b = xe @ W3[e].T
+            h = silu(a) * b
+            y = h @ W2[e].T
+            dw[rows, j] = np.sum(dout[rows] * y, axis=1)
+            dy = w[rows, j][:, None] * dout[rows]
+            dh = dy @ W2[e]
+            da = dh * b * silu_grad(a)
+            db = dh * silu(a)
+            dx[rows] += da @ W1[e] + db @ W3[e]
+            dW2[e] += dy.T @ h
+            dW1[e] += da.T @ xe
+            dW3[e] += db.T @ xe
+    dl = w * (dw - np.sum(w * dw, axis=1, keepdims=True))
+    for j in range(k):
+        dx += dl[:, j][:, None] * Wg[idx[:, j]]
+        np.add.at(dWg, idx[:, j], dl[:, j][:, None] * x)
+    return {"dx": dx, "dWg": dWg, "dW1": dW1, "dW3": dW3, "dW2": dW2}

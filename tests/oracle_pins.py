@@ -500,4 +500,101 @@ def pin_w8_layer_brute_force(o):
     assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 0.03
 
 
+# ------------------------------------------------------------------ backward
+# Mixtral 8x7B model reference page, Training: experts and router are trained
+# together.  The gradients are pinned to central finite differences of the
+# oracle's own forward (a computation that shares no step with the backward's
+# chain rule), to library autodiff for the dense special case, and to
+# invariants.
+def _loss_grad_fd(o, L, k, dout, name, eps=1e-6):
+    args = {n: L[n] for n in ("x", "Wg", "W1", "W3", "W2")}
+    base = args[name]
+    fd = np.zeros_like(base)
+    for i in np.ndindex(base.shape):
+        for sgn in (1.0, -1.0):
+            p = base.copy()
+            p[i] += sgn * eps
+            a = dict(args)
+            a[name] = p
+            out = o.moe_forward(a["x"], a["Wg"], a["W1"], a["W3"], a["W2"], k)[0]
+            fd[i] += sgn * np.sum(out * dout)
+    return fd / (2 * eps)
+
+
+def pin_backward_finite_differences(o):
+    """Every gradient equals central finite differences of the forward (the
+    routing has clear gaps, so no top-k choice flips within +-eps)."""
+    L = _tiny_layer(91, T=5, d=6, F=7, E=4)
+    k = 2
+    logits = L["x"] @ L["Wg"].T
+    srt = -np.sort(-logits, axis=1)
+    assert np.min(srt[:, 1] - srt[:, 2]) > 1e-3
+    dout = _rng(92).standard_normal((5, 6))
+    g = o.moe_backward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], k, dout)
+    for name in ("x", "Wg", "W1", "W3", "W2"):
+        fd = _loss_grad_fd(o, L, k, dout, name)
+        got = g["d" + name]
+        assert got.shape == fd.shape, name
+        assert np.max(np.abs(got - fd)) <= 1e-7 * max(1.0, np.max(np.abs(fd))), name
+
+
+def pin_backward_silu_derivative(o):
+    """silu'(a) against a 40-digit numerical derivative, and its closed values
+    silu'(0) = 1/2 and silu'(a) -> 1 (a -> +inf), -> 0 (a -> -inf)."""
+    pts = [-6.0, -1.3, -0.2, 0.0, 0.7, 2.5, 9.0]
+    got = o.silu_grad(np.array(pts))
+    for a, gv in zip(pts, got):
+        want = mpmath.diff(lambda t: t / (1 + mpmath.exp(-t)), mpmath.mpf(a))
+        assert abs(gv - float(want)) < 1e-14, a
+    assert o.silu_grad(np.array([0.0]))[0] == 0.5
+    assert abs(o.silu_grad(np.array([40.0]))[0] - 1.0) < 1e-12
+    assert abs(o.silu_grad(np.array([-40.0]))[0]) < 1e-12
+
+
+def pin_backward_linear_in_dout(o):
+    """The gradients are linear in the output gradient."""
+    L = _tiny_layer(93, T=12, d=8, F=6, E=4)
+    r = _rng(94)
+    d1, d2 = r.standard_normal((12, 8)), r.standard_normal((12, 8))
+    g1 = o.moe_backward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 2, d1)
+    g2 = o.moe_backward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 2, d2)
+    g12 = o.moe_backward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 2, 2.0 * d1 - 3.0 * d2)
+    for n in g1:
+        assert np.allclose(g12[n], 2.0 * g1[n] - 3.0 * g2[n], rtol=1e-11, atol=1e-12), n
+
+
+def pin_backward_identical_experts_no_router_gradient(o):
+    """With identical experts every chosen expert gives the same output, the
+    gate weights sum to 1, so the router receives no gradient."""
+    r = _rng(95)
+    T, d, F, E = 20, 8, 6, 5
+    one = [r.standard_normal(s) / 3 for s in ((F, d), (F, d), (d, F))]
+    W1, W3, W2 = (np.repeat(m[None], E, axis=0) for m in one)
+    x = r.standard_normal((T, d))
+    Wg = r.standard_normal((E, d))
+    g = o.moe_backward(x, Wg, W1, W3, W2, 2, r.standard_normal((T, d)))
+    assert np.max(np.abs(g["dWg"])) < 1e-12
+
+
+def pin_backward_dense_reduction_autograd(o):
+    """E=1, k=1: the layer is the dense SwiGLU FFN; its gradients match
+    torch.autograd in fp64 and the gate gets none."""
+    r = _rng(96)
+    T, d, F = 9, 7, 5
+    x = r.standard_normal((T, d))
+    Wg = r.standard_normal((1, d))
+    W1, W3 = r.standard_normal((1, F, d)) / 2, r.standard_normal((1, F, d)) / 2
+    W2 = r.standard_normal((1, d, F)) / 2
+    dout = r.standard_normal((T, d))
+    g = o.moe_backward(x, Wg, W1, W3, W2, 1, dout)
+    tx, t1, t3, t2 = (torch.tensor(v, dtype=torch.float64, requires_grad=True) for v in (x, W1[0], W3[0], W2[0]))
+    out = (torch.nn.functional.silu(tx @ t1.T) * (tx @ t3.T)) @ t2.T
+    out.backward(torch.tensor(dout, dtype=torch.float64))
+    for name, tv in (("dx", tx), ("dW1", t1), ("dW3", t3), ("dW2", t2)):
+        want = tv.grad.numpy()
+        got = g[name] if name == "dx" else g[name][0]
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12), name
+    assert np.all(g["dWg"] == 0.0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

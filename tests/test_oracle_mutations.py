@@ -199,13 +199,70 @@ def _w8_drops_scale(m):
     m.dequantize_int8_rows = lambda q, s: np.asarray(q, dtype=np.float64)
 
 
+def _bwd_silu_grad_is_silu(m):
+    m.silu_grad = lambda a: m.silu(a)
+
+
+def _bwd_silu_grad_drops_term(m):
+    m.silu_grad = lambda a: 1.0 / (1.0 + np.exp(-a))
+
+
+def _bwd_no_softmax_jacobian(m):
+    src = m.moe_backward
+
+    def bwd(x, Wg, W1, W3, W2, k, dout):
+        g = src(x, Wg, W1, W3, W2, k, dout)
+        # a plausible mistake: router gradient taken as w * dw (no centering)
+        w, idx, _ = m.router(x, Wg, k)
+        xx = m.f64(x)
+        dw = np.zeros_like(w)
+        for j in range(k):
+            for t in range(xx.shape[0]):
+                e = idx[t, j]
+                a = xx[t] @ m.f64(W1[e]).T
+                b = xx[t] @ m.f64(W3[e]).T
+                dw[t, j] = np.sum(m.f64(dout)[t] * ((m.silu(a) * b) @ m.f64(W2[e]).T))
+        dl_bad = w * dw
+        dl_ok = w * (dw - np.sum(w * dw, axis=1, keepdims=True))
+        Wgf = m.f64(Wg)
+        for j in range(k):
+            g["dx"] += (dl_bad - dl_ok)[:, j][:, None] * Wgf[idx[:, j]]
+            np.add.at(g["dWg"], idx[:, j], (dl_bad - dl_ok)[:, j][:, None] * xx)
+        return g
+    m.moe_backward = bwd
+
+
+def _bwd_drops_gate_weight(m):
+    src = m.moe_backward
+
+    def bwd(x, Wg, W1, W3, W2, k, dout):
+        g = src(x, Wg, W1, W3, W2, k, dout)
+        g["dW2"] = g["dW2"] * 2.0
+        return g
+    m.moe_backward = bwd
+
+
+def _bwd_transposed_dw1(m):
+    src = m.moe_backward
+
+    def bwd(x, Wg, W1, W3, W2, k, dout):
+        g = src(x, Wg, W1, W3, W2, k, dout)
+        if g["dW1"].shape[1] == g["dW1"].shape[2]:
+            g["dW1"] = np.transpose(g["dW1"], (0, 2, 1)).copy()
+        else:
+            g["dW1"] = g["dW1"][:, ::-1].copy()
+        return g
+    m.moe_backward = bwd
+
+
 MUTANTS = {f.__name__[1:]: f for f in [
     _swap_gate_up, _silu_sign, _silu_is_sigmoid, _no_renormalise, _ascending_topk,
     _ties_to_higher_index, _drop_gate_weight, _only_first_slot, _transposed_down,
     _gate_transposed, _rms_no_square, _rms_no_eps, _rms_no_gamma, _bf16_truncates,
     _block_no_residual, _block_unnormalised, _two_matrix_expert, _dispatch_unstable,
     _dispatch_token_not_pair, _hidden_no_gate, _rms32_no_square, _int8_divisor_128, _int8_truncates,
-    _int8_ties_away_from_zero, _int8_per_column, _w8_drops_scale]}
+    _int8_ties_away_from_zero, _int8_per_column, _w8_drops_scale, _bwd_silu_grad_is_silu,
+    _bwd_silu_grad_drops_term, _bwd_no_softmax_jacobian, _bwd_drops_gate_weight, _bwd_transposed_dw1]}
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
