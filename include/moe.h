@@ -241,6 +241,38 @@ int moe_forward_w8(const void* x, const void* Wg, const int8_t* W1q, const float
                    int k, moe_stream_t stream);
 
 /*
+ * ---- backward (training) ------------------------------------------------
+ * Mixtral 8x7B model reference page, Training: the experts and the router are
+ * trained together.  For L = sum(out * dout), out = the bf16 layer, these
+ * calls compute dL/dx, dL/dWg, dL/dW1, dL/dW3, dL/dW2.  The top-k choice is
+ * piecewise constant, so the router receives its gradient through the softmax
+ * over the k chosen logits only:
+ *   dy_j = w_j dout,  dw_j = <dout, y_j>,  dl_j = w_j (dw_j - sum_i w_i dw_i)
+ *   dh = dy W2_e,  da = dh * b * silu'(a),  db = dh * silu(a)  (a = x W1_e^T, b = x W3_e^T)
+ *   dx = sum_j (da W1_e + db W3_e) + sum_j dl_j Wg[i_j]
+ *   dW2_e = sum dy^T h,  dW1_e = sum da^T x,  dW3_e = sum db^T x,  dWg[i_j] += dl_j x
+ * Inputs: dout[T,d] bf16 and the forward's inputs.  `saved` is the scratch
+ * that moe_forward_ws(x, Wg, W1, W3, W2, out, ..., MOE_DTYPE_BF16, saved,
+ * saved_bytes, ...) filled for the same inputs, unmodified since (it holds
+ * the routing, the permutation, x_perm, h and y_perm).  Outputs (overwritten):
+ * dx[T,d] bf16; dWg[E,d], dW1[E,dff,d], dW3[E,dff,d], dW2[E,d,dff] fp32 (an
+ * expert no token chose gets zeros).  dh is formed in fp32 from the exact
+ * dout rows and the fp32 gate weight; the intermediates da, db, the permuted
+ * dx and (for dW2 only) dy are bf16; every GEMM accumulates in fp32 on the
+ * tensor cores.
+ * Shapes as the bf16 forward.  The block form is not differentiated here.
+ */
+size_t moe_backward_workspace_bytes(int T, int d, int dff, int E, int k);
+int moe_backward_ws(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3,
+                    const void* W2, const void* saved, size_t saved_bytes, void* dx, float* dWg, float* dW1,
+                    float* dW3, float* dW2, int T, int d, int dff, int E, int k, void* workspace,
+                    size_t workspace_bytes, moe_stream_t stream);
+/* As moe_backward_ws, scratch from cudaMallocAsync on `stream`. */
+int moe_backward(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                 const void* saved, size_t saved_bytes, void* dx, float* dWg, float* dW1, float* dW3, float* dW2,
+                 int T, int d, int dff, int E, int k, moe_stream_t stream);
+
+/*
  * Scratch size built into moe_forward_noalloc (16 MiB per GPU).
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -269,8 +269,16 @@ def silu_grad(a) -> np.ndarray:
     return s * (1.0 + a * (1.0 - s))
 
 
-def moe_backward(x, Wg, W1, W3, W2, k, dout):
+def moe_backward(x, Wg, W1, W3, W2, k, dout, idx=None, experts=None, with_scale=False):
     """Gradients of L = sum(out * dout) for out = moe_forward(x, ...).
+
+    ``idx`` replaces the router's choice (the weights are then the softmax
+    over the chosen logits), for scoring near-tie tokens; ``experts`` limits
+    the expert weight gradients to those experts (the others stay zero), to
+    bound memory at full size.  ``with_scale`` also returns, under the same
+    keys with a "_scale" suffix, each output's sum of the absolute values of
+    the terms it is summed from (through the chain), the quantity rounding-
+    error bounds of a computation with rounded factors are proportional to.
 
     Returns dict(dx[T,d], dWg[E,d], dW1[E,F,d], dW3[E,F,d], dW2[E,d,F]) in fp64,
     following the chain rule step by step:
@@ -283,35 +291,61 @@ def moe_backward(x, Wg, W1, W3, W2, k, dout):
     """
     x = f64(x)
     dout = f64(dout)
-    W1, W3, W2, Wg = f64(W1), f64(W3), f64(W2), f64(Wg)
+    Wg = f64(Wg)
     T, d = x.shape
-    E = W1.shape[0]
-    w, idx, _ = router(x, Wg, k)
+    E, F = W1.shape[0], W1.shape[1]
+    if idx is None:
+        w, idx, _ = router(x, Wg, k)
+    else:
+        idx = np.asarray(idx)
+        w = softmax(np.take_along_axis(router_logits(x, Wg), idx, axis=1))
+    keep = set(range(E)) if experts is None else set(experts)
     dx = np.zeros_like(x)
     dWg = np.zeros_like(Wg)
-    dW1, dW3, dW2 = np.zeros_like(W1), np.zeros_like(W3), np.zeros_like(W2)
+    dW1, dW3, dW2 = np.zeros((E, F, d)), np.zeros((E, F, d)), np.zeros((E, d, F))
     dw = np.zeros((T, k))
+    if with_scale:
+        sx, sWg = np.zeros_like(x), np.zeros_like(Wg)
+        s1, s3, s2 = np.zeros((E, F, d)), np.zeros((E, F, d)), np.zeros((E, d, F))
+        sdw = np.zeros((T, k))
     for j in range(k):
         for e in range(E):
             rows = np.nonzero(idx[:, j] == e)[0]
             if rows.size == 0:
                 continue
             xe = x[rows]
-            a = xe @ W1[e].T
-            b = xe @ W3[e].T
+            W1e, W3e, W2e = f64(W1[e]), f64(W3[e]), f64(W2[e])
+            a = xe @ W1e.T
+            b = xe @ W3e.T
             h = silu(a) * b
-            y = h @ W2[e].T
+            y = h @ W2e.T
             dw[rows, j] = np.sum(dout[rows] * y, axis=1)
             dy = w[rows, j][:, None] * dout[rows]
-            dh = dy @ W2[e]
+            dh = dy @ W2e
             da = dh * b * silu_grad(a)
             db = dh * silu(a)
-            dx[rows] += da @ W1[e] + db @ W3[e]
-            dW2[e] += dy.T @ h
-            dW1[e] += da.T @ xe
-            dW3[e] += db.T @ xe
+            dx[rows] += da @ W1e + db @ W3e
+            if e in keep:
+                dW2[e] += dy.T @ h
+                dW1[e] += da.T @ xe
+                dW3[e] += db.T @ xe
+            if with_scale:
+                sdw[rows, j] = np.sum(np.abs(dout[rows] * y), axis=1)
+                ada, adb, axe = np.abs(da), np.abs(db), np.abs(xe)
+                sx[rows] += ada @ np.abs(W1e) + adb @ np.abs(W3e)
+                if e in keep:
+                    s2[e] += np.abs(dy).T @ np.abs(h)
+                    s1[e] += ada.T @ axe
+                    s3[e] += adb.T @ axe
     dl = w * (dw - np.sum(w * dw, axis=1, keepdims=True))
     for j in range(k):
         dx += dl[:, j][:, None] * Wg[idx[:, j]]
         np.add.at(dWg, idx[:, j], dl[:, j][:, None] * x)
-    return {"dx": dx, "dWg": dWg, "dW1": dW1, "dW3": dW3, "dW2": dW2}
+    out = {"dx": dx, "dWg": dWg, "dW1": dW1, "dW3": dW3, "dW2": dW2}
+    if with_scale:
+        sdl = w * (sdw + np.sum(w * sdw, axis=1, keepdims=True))
+        for j in range(k):
+            sx += sdl[:, j][:, None] * np.abs(Wg[idx[:, j]])
+            np.add.at(sWg, idx[:, j], sdl[:, j][:, None] * np.abs(x))
+        out.update({"dx_scale": sx, "dWg_scale": sWg, "dW1_scale": s1, "dW3_scale": s3, "dW2_scale": s2})
+    return out

@@ -52,6 +52,9 @@ SIGNATURES = {
     "moe_expert_down_w8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "moe_forward_w8_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_forward_w8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "moe_backward_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_backward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "moe_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_get_device_status": (_I, [_P, ctypes.POINTER(_I), _I]),
     "moe_set_wait_limit_ns": (_I, [_LL]),
@@ -367,6 +370,48 @@ def moe_forward_w8(x, Wg, W1q, W1s, W3q, W3s, W2q, W2s, k, out=None, stream=None
     _check("moe_forward_w8", lib().moe_forward_w8(_p(x), _p(Wg), _p(W1q), _p(W1s), _p(W3q), _p(W3s), _p(W2q),
                                                   _p(W2s), _p(out), T, d, dff, E, k, _stream(stream)))
     return out
+
+
+# ------------------------------------------------------------------ backward
+def moe_backward_workspace_bytes(T, d, dff, E, k) -> int:
+    return int(lib().moe_backward_workspace_bytes(T, d, dff, E, k))
+
+
+def _grads(x, Wg, W1, W3, W2, grads):
+    if grads is not None:
+        return grads
+    dev = x.device
+    return {"dx": torch.empty_like(x), "dWg": torch.empty(Wg.shape, dtype=torch.float32, device=dev),
+            "dW1": torch.empty(W1.shape, dtype=torch.float32, device=dev),
+            "dW3": torch.empty(W3.shape, dtype=torch.float32, device=dev),
+            "dW2": torch.empty(W2.shape, dtype=torch.float32, device=dev)}
+
+
+def moe_backward_ws(dout, x, Wg, W1, W3, W2, k, saved, ws, grads=None, stream=None):
+    """Backward of the bf16 layer.  `saved` is the uint8 scratch the forward
+    (moe_forward_ws) used on the same inputs; `ws` the backward's scratch.
+    Returns dict(dx, dWg, dW1, dW3, dW2)."""
+    _dev(dout, x, Wg, W1, W3, W2, saved, ws)
+    T, d = x.shape
+    E, dff, _ = W1.shape
+    g = _grads(x, Wg, W1, W3, W2, grads)
+    _check("moe_backward_ws", lib().moe_backward_ws(_p(dout), _p(x), _p(Wg), _p(W1), _p(W3), _p(W2), _p(saved),
+                                                    saved.numel(), _p(g["dx"]), _p(g["dWg"]), _p(g["dW1"]),
+                                                    _p(g["dW3"]), _p(g["dW2"]), T, d, dff, E, k, _p(ws), ws.numel(),
+                                                    _stream(stream)))
+    return g
+
+
+def moe_backward(dout, x, Wg, W1, W3, W2, k, saved, grads=None, stream=None):
+    """As moe_backward_ws with scratch from the stream-ordered pool."""
+    _dev(dout, x, Wg, W1, W3, W2, saved)
+    T, d = x.shape
+    E, dff, _ = W1.shape
+    g = _grads(x, Wg, W1, W3, W2, grads)
+    _check("moe_backward", lib().moe_backward(_p(dout), _p(x), _p(Wg), _p(W1), _p(W3), _p(W2), _p(saved),
+                                              saved.numel(), _p(g["dx"]), _p(g["dWg"]), _p(g["dW1"]), _p(g["dW3"]),
+                                              _p(g["dW2"]), T, d, dff, E, k, _stream(stream)))
+    return g
 
 
 def moe_forward_noalloc(x, Wg, W1, W3, W2, k, out=None, stream=None):

@@ -261,6 +261,107 @@ int forward_w8(const void* x, const void* Wg, const W8Weights& w8, void* out, in
   return fe == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 
+
+// ---- backward ---------------------------------------------------------------
+struct BwdLayout {
+  size_t dy, dop, wp, dl, dA, dB, dxp, W2t, W1t, W3t, Xt, dYt, Ht, dAt, dBt, part, total;
+  size_t kp;
+};
+
+BwdLayout bwd_layout(int T, int d, int dff, int E, int k) {
+  const size_t Tk = static_cast<size_t>(T) * k;
+  const size_t kp = bwd_kpad_cols(static_cast<int>(Tk), E);
+  const size_t wsz = static_cast<size_t>(E) * dff * d * 2;
+  BwdLayout L;
+  size_t o = 0;
+  L.kp = kp;
+  L.dy = o;    o = al256(o + Tk * d * 2);
+  L.dop = o;   o = al256(o + Tk * d * 2);
+  L.wp = o;    o = al256(o + Tk * 4);
+  L.dl = o;    o = al256(o + Tk * 4);
+  L.dA = o;    o = al256(o + Tk * dff * 2);
+  L.dB = o;    o = al256(o + Tk * dff * 2);
+  L.dxp = o;   o = al256(o + Tk * d * 2);
+  L.W2t = o;   o = al256(o + wsz);
+  L.W1t = o;   o = al256(o + wsz);
+  L.W3t = o;   o = al256(o + wsz);
+  L.Xt = o;    o = al256(o + kp * d * 2);
+  L.dYt = o;   o = al256(o + kp * d * 2);
+  L.Ht = o;    o = al256(o + kp * dff * 2);
+  L.dAt = o;   o = al256(o + kp * dff * 2);
+  L.dBt = o;   o = al256(o + kp * dff * 2);
+  L.part = o;  o = al256(o + static_cast<size_t>(dwg_chunks(T)) * E * d * 4);
+  L.total = o;
+  return L;
+}
+
+// The backward, B1..B8, on caller scratch; `saved` is the scratch of the
+// forward call (moe_forward_ws) on the same x and weights.
+int backward_impl(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                  const void* saved, void* dx, float* dWg, float* dW1, float* dW3, float* dW2, int T, int d, int dff,
+                  int E, int k, void* ws, const Ctx& c, cudaStream_t s) {
+  const WsLayout F = ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16);
+  const BwdLayout L = bwd_layout(T, d, dff, E, k);
+  const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  const int32_t* idx = reinterpret_cast<const int32_t*>(sv + F.idx);
+  const float* w = reinterpret_cast<const float*>(sv + F.w);
+  const int32_t* offs = reinterpret_cast<const int32_t*>(sv + F.offs);
+  const int32_t* slot_pos = reinterpret_cast<const int32_t*>(sv + F.slot_pos);
+  const void* x_perm = sv + F.x_perm;
+  const void* h = sv + F.h;
+  const void* y_perm = sv + F.y;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  void* dy = b + L.dy;
+  void* dop = b + L.dop;
+  float* wp = reinterpret_cast<float*>(b + L.wp);
+  float* dl = reinterpret_cast<float*>(b + L.dl);
+  void* dA = b + L.dA;
+  void* dB = b + L.dB;
+  void* dxp = b + L.dxp;
+  const int Tk = T * k;
+  const int kp = static_cast<int>(L.kp);
+  // B1-B2: expert-output and gate-weight gradients, softmax over the k chosen.
+  MOE_TRY(launch_rc(launch_route_bwd(dout, y_perm, slot_pos, w, dy, dop, wp, dl, T, d, k, c, s)));
+  // K-major copies of the weights for the input-gradient GEMMs.
+  MOE_TRY(launch_rc(launch_transpose_batched(W2, b + L.W2t, E, d, dff, s)));
+  MOE_TRY(launch_rc(launch_transpose_batched(W1, b + L.W1t, E, dff, d, s)));
+  MOE_TRY(launch_rc(launch_transpose_batched(W3, b + L.W3t, E, dff, d, s)));
+  // B3: dh = w (dout W2), a and b recomputed, SwiGLU derivative -> dA, dB.
+  MOE_TRY(launch_bwd_dswiglu(dop, wp, x_perm, offs, b + L.W2t, W1, W3, dA, dB, Tk, d, dff, E, c, s));
+  // B4: dx_perm = dA W1 + dB W3.
+  MOE_TRY(launch_bwd_dx(dA, dB, offs, b + L.W1t, b + L.W3t, dxp, Tk, d, dff, E, c, s));
+  // B5: un-permute + router path -> dx.
+  MOE_TRY(launch_rc(launch_dx_gather(dxp, slot_pos, idx, dl, Wg, dx, T, d, E, k, c, s)));
+  // B6: dWg.
+  MOE_TRY(launch_rc(launch_dwg(x, idx, dl, reinterpret_cast<float*>(b + L.part), dWg, T, d, E, k, c, s)));
+  // B7: token-major -> [channels, padded tokens] for the weight gradients.
+  MOE_TRY(launch_rc(launch_transpose_segments(x_perm, offs, b + L.Xt, Tk, d, kp, E, s)));
+  MOE_TRY(launch_rc(launch_transpose_segments(dy, offs, b + L.dYt, Tk, d, kp, E, s)));
+  MOE_TRY(launch_rc(launch_transpose_segments(h, offs, b + L.Ht, Tk, dff, kp, E, s)));
+  MOE_TRY(launch_rc(launch_transpose_segments(dA, offs, b + L.dAt, Tk, dff, kp, E, s)));
+  MOE_TRY(launch_rc(launch_transpose_segments(dB, offs, b + L.dBt, Tk, dff, kp, E, s)));
+  // B8: dW2 = dy^T h, dW1 = dA^T x, dW3 = dB^T x per expert.
+  MOE_TRY(launch_bwd_wgrad(b + L.dYt, b + L.Ht, offs, dW2, d, dff, Tk, E, c, s));
+  MOE_TRY(launch_bwd_wgrad(b + L.dAt, b + L.Xt, offs, dW1, dff, d, Tk, E, c, s));
+  MOE_TRY(launch_bwd_wgrad(b + L.dBt, b + L.Xt, offs, dW3, dff, d, Tk, E, c, s));
+  return MOE_OK;
+}
+
+int check_backward(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                   const void* saved, size_t saved_bytes, const void* dx, const float* dWg, const float* dW1,
+                   const float* dW3, const float* dW2, int T, int d, int dff, int E, int k) {
+  MOE_TRY(check_forward(x, Wg, W1, W3, W2, dx, T, d, dff, E, k, MOE_DTYPE_BF16));
+  if (T == 0) return MOE_OK;
+  if (static_cast<long long>(E) * dff * d > INT_MAX || static_cast<long long>(T) * k * dff > (1LL << 40))
+    return MOE_EUNSUPPORTED;
+  const void* ptrs[] = {dout, saved, dWg, dW1, dW3, dW2};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
+  if (!aligned(saved, 256)) return MOE_EINVAL;
+  if (saved_bytes < ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16).total) return MOE_ENOMEM;
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -494,6 +595,43 @@ int moe_forward_w8(const void* x, const void* Wg, const int8_t* W1q, const float
                    int k, moe_stream_t stream) {
   const W8Weights w8{W1q, W1s, W3q, W3s, W2q, W2s};
   return forward_w8(x, Wg, w8, out, T, d, dff, E, k, nullptr, 0, true, stream);
+}
+
+size_t moe_backward_workspace_bytes(int T, int d, int dff, int E, int k) {
+  if (check_tokens(T, d, E, k, MOE_DTYPE_BF16) != MOE_OK || dff <= 0) return 0;
+  return bwd_layout(T, d, dff, E, k).total;
+}
+
+int moe_backward_ws(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                    const void* saved, size_t saved_bytes, void* dx, float* dWg, float* dW1, float* dW3, float* dW2,
+                    int T, int d, int dff, int E, int k, void* workspace, size_t workspace_bytes,
+                    moe_stream_t stream) {
+  MOE_TRY(check_backward(dout, x, Wg, W1, W3, W2, saved, saved_bytes, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k));
+  if (T == 0) return MOE_OK;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
+  if (workspace_bytes < bwd_layout(T, d, dff, E, k).total) return MOE_ENOMEM;
+  Ctx c;
+  MOE_TRY(make_ctx(dx, &c));
+  return backward_impl(dout, x, Wg, W1, W3, W2, saved, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k, workspace, c, stream);
+}
+
+int moe_backward(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                 const void* saved, size_t saved_bytes, void* dx, float* dWg, float* dW1, float* dW3, float* dW2,
+                 int T, int d, int dff, int E, int k, moe_stream_t stream) {
+  MOE_TRY(check_backward(dout, x, Wg, W1, W3, W2, saved, saved_bytes, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k));
+  if (T == 0) return MOE_OK;
+  Ctx c;
+  MOE_TRY(make_ctx(dx, &c));
+  const size_t bytes = bwd_layout(T, d, dff, E, k).total;
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ENOMEM;
+  }
+  const int rc = backward_impl(dout, x, Wg, W1, W3, W2, saved, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k, ws, c, stream);
+  const cudaError_t fe = cudaFreeAsync(ws, stream);
+  if (rc != MOE_OK) return rc;
+  return fe == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 
 int moe_get_device_status(moe_stream_t stream, int* status, int reset) {

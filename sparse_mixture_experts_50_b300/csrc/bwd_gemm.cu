@@ -1,0 +1,579 @@
+// Backward of the expert GEMMs (Mixtral 8x7B model reference page, Training:
+// the experts and the router are trained together; "The Evolving
+// Transformer - 05 Mixtral", section 04, SwiGLU: y = W2 (silu(W1 x) * W3 x)).
+// For the rows p of expert e, with dout gathered per routed row and w_p the
+// row's gate weight:
+//   dh = w_p (dout W2_e),  a = x W1_e^T,  b = x W3_e^T,
+//   da = dh * b * silu'(a),  db = dh * silu(a)                    (DSWIGLU)
+//   dx_perm = da W1_e + db W3_e                                    (DX)
+//   dW2_e = dy^T h,  dW1_e = da^T x,  dW3_e = db^T x               (WGRAD)
+//
+// One persistent tcgen05 kernel template, one CTA per SM, warp-specialised
+// like the forward kernel (warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5
+// epilogue), every operand K-major and staged by TMA with the 128-byte
+// swizzle.  The weight operands of DSWIGLU and DX are the transposed copies
+// W2t [E,F,d], W1t and W3t [E,d,F]; WGRAD reads token-major activations
+// transposed to [channels, tokens] with each expert's tokens padded to a
+// multiple of 64 (zeros), so that every K step of an expert starts on a
+// 128-byte boundary.
+//   DSWIGLU  tile 128 rows x 128 h columns; three K=d passes accumulate
+//            dout W2, a and b into three 128-column accumulators (tensor
+//            memory columns 0-383); the epilogue scales the first by w_p in
+//            fp32 (dout is gathered exactly, so dh is not exposed to a bf16
+//            rounding of w dout, which its 4096-term sum can amplify where
+//            it cancels), forms da, db in fp32 and rounds them to bf16.  a
+//            and b are recomputed, not saved.
+//   DX       tile 128 rows x 256 columns of dx_perm; two K=F passes (da with
+//            W1t, then db with W3t) into one accumulator; two accumulators
+//            alternate between tiles.
+//   WGRAD    per expert an [M, N] fp32 matrix, tile 128 x 256, K = the
+//            expert's padded token segment; an expert with no tokens gets
+//            zeros (its tiles skip the MMAs).
+// Every wait is bounded as in the forward kernel.
+#include <cuda.h>
+#include <mutex>
+
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+enum { MODE_DSWIGLU = 0, MODE_DX = 1, MODE_WGRAD = 2 };
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int BNH = 128;                  // one B box
+constexpr int UMMA_K = 16;
+constexpr int A_BYTES = BM * BK * 2;      // 16 KB
+constexpr int B_BYTES = 2 * BNH * BK * 2; // up to two B boxes, 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int EPI_THREADS = 128;
+constexpr int MAX_E = 64;
+constexpr int KPAD = 64;                  // WGRAD: token segments padded to this
+
+struct Ctl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int tile_prefix[MAX_E + 1];
+  int mtiles[MAX_E];
+  int seg[MAX_E + 1];    // row segments (M-grouped) / padded token segments (WGRAD)
+  int rows[MAX_E];       // WGRAD: real tokens of each expert
+};
+
+constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(Ctl);
+
+struct BwdArgs {
+  const int32_t* offsets;  // [E+1] routed-row boundaries
+  int E;
+  int Tk;
+  int K;                   // reduction length of one pass (d, F; WGRAD: unused)
+  int b_rows;              // rows per expert in the B tensor(s)
+  int n_out;               // output columns (DSWIGLU: F, DX: d, WGRAD: N)
+  int m_rows;              // WGRAD: output rows M
+  int n_tiles;
+  // DSWIGLU: out0 = dA, out1 = dB [Tk, F]; DX: out0 = dx_perm [Tk, d]
+  __nv_bfloat16* out0;
+  __nv_bfloat16* out1;
+  float* outf;             // WGRAD: [E, M, N]
+  const float* w_perm;     // DSWIGLU: gate weight of each routed row [Tk]
+  int* status;
+  unsigned long long wait_ns;
+};
+
+constexpr uint64_t kDrainFloorNs = 2000000000ull;
+__device__ __forceinline__ uint64_t drain_limit(uint64_t w) { return w > kDrainFloorNs ? w : kDrainFloorNs; }
+
+__device__ __forceinline__ void raise_abort(Ctl* ctl, int* status) {
+  *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+  record_status(status, MOE_ETIMEOUT);
+}
+
+__device__ __forceinline__ void decode_tile(const Ctl* ctl, int E, int tile, int& e, int& m, int& n) {
+  e = 0;
+  while (e + 1 < E && ctl->tile_prefix[e + 1] <= tile) ++e;
+  const int local = tile - ctl->tile_prefix[e];
+  const int mt = ctl->mtiles[e];
+  n = local / mt;
+  m = local - n * mt;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int MODE>
+struct Shape {
+  static constexpr int passes = MODE == MODE_DSWIGLU ? 3 : (MODE == MODE_DX ? 2 : 1);
+  static constexpr int n_tile = MODE == MODE_DSWIGLU ? BNH : 2 * BNH;   // output columns per tile
+  static constexpr int b_boxes = MODE == MODE_DSWIGLU ? 1 : 2;
+  static constexpr int acc_cols = MODE == MODE_DSWIGLU ? 3 * BNH : 2 * BNH;
+  static constexpr int n_acc = MODE == MODE_DSWIGLU ? 1 : 2;             // accumulators in flight
+  static constexpr int tmem_cols = 512;
+  static constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, b_boxes * BNH);
+};
+
+// Tensor maps per pass: A (token rows or, WGRAD, channel rows) and B.
+struct Maps {
+  CUtensorMap a[3];
+  CUtensorMap b[3];
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_constant__ Maps maps, const BwdArgs args) {
+  using S = Shape<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const volatile int* abort_flag = &ctl->abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&ctl->full[s], 1);
+      ptx::mbar_init(&ctl->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&ctl->tfull[a], 1);
+      ptx::mbar_init(&ctl->tempty[a], EPI_THREADS);
+    }
+    ptx::mbar_init(&ctl->drain, 1);
+    ctl->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int p = 0; p < S::passes; ++p) {
+      ptx::prefetch_tmap(&maps.a[p]);
+      ptx::prefetch_tmap(&maps.b[p]);
+    }
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl->tmem_base, S::tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  pdl_enter();
+  if (threadIdx.x == 0) {
+    int prev = 0;
+    int run = 0;
+    int kseg = 0;
+    ctl->tile_prefix[0] = 0;
+    for (int e = 0; e <= args.E; ++e) {
+      int o = args.offsets[e];
+      if (o < prev || o > args.Tk) {
+        record_status(args.status, MOE_EDEVICE);
+        o = prev;
+      }
+      if (e > 0) {
+        const int n_e = o - prev;
+        if (MODE == MODE_WGRAD) {
+          ctl->rows[e - 1] = n_e;
+          ctl->seg[e - 1] = kseg;
+          kseg += (n_e + KPAD - 1) / KPAD * KPAD;
+          const int mt = (args.m_rows + BM - 1) / BM;
+          ctl->mtiles[e - 1] = mt;
+          run += mt * args.n_tiles;
+        } else {
+          ctl->seg[e - 1] = prev;
+          const int mt = (n_e + BM - 1) / BM;
+          ctl->mtiles[e - 1] = mt;
+          run += mt * args.n_tiles;
+        }
+        ctl->tile_prefix[e] = run;
+      }
+      prev = o;
+    }
+    ctl->seg[args.E] = MODE == MODE_WGRAD ? kseg : prev;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int total_tiles = ctl->tile_prefix[args.E];
+  const int kb_pass = (args.K + BK - 1) / BK;
+
+  // K steps of a tile (all passes).
+  auto tile_kblocks = [&](int e) -> int {
+    if (MODE == MODE_WGRAD) return (ctl->seg[e + 1] - ctl->seg[e]) / BK;
+    return S::passes * kb_pass;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0;
+      uint32_t last_parity[STAGES];
+      for (int s = 0; s < STAGES; ++s) last_parity[s] = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        int e, m, n;
+        decode_tile(ctl, args.E, tile, e, m, n);
+        const int nkb = tile_kblocks(e);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, args.wait_ns)) {
+            raise_abort(ctl, args.status);
+            ok = false;
+            break;
+          }
+          int pass, kx, arow, brow;
+          if (MODE == MODE_WGRAD) {
+            pass = 0;
+            kx = ctl->seg[e] + kb * BK;
+            arow = m * BM;
+            brow = n * 2 * BNH;
+          } else {
+            pass = kb / kb_pass;
+            kx = (kb - pass * kb_pass) * BK;
+            arow = ctl->seg[e] + m * BM;
+            brow = e * args.b_rows + n * S::n_tile;
+          }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          constexpr int bytes = A_BYTES + S::b_boxes * BNH * BK * 2;
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage], bytes);
+          ptx::tma_load_2d(sa, &maps.a[pass], &ctl->full[stage], kx, arow);
+          ptx::tma_load_2d(sa + A_BYTES, &maps.b[pass], &ctl->full[stage], kx, brow);
+          if (S::b_boxes == 2)
+            ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[pass], &ctl->full[stage], kx, brow + BNH);
+          filled |= 1u << stage;
+          last_parity[stage] = phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < STAGES; ++s) {
+        if (filled & (1u << s)) ptx::mbar_wait(&ctl->full[s], last_parity[s], nullptr, drain_limit(args.wait_ns));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        int e, m, n;
+        decode_tile(ctl, args.E, tile, e, m, n);
+        const int nkb = tile_kblocks(e);
+        if (!ptx::mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, abort_flag, args.wait_ns)) {
+          raise_abort(ctl, args.status);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::acc_cols);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag, args.wait_ns)) {
+            raise_abort(ctl, args.status);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          // DSWIGLU: pass p accumulates into its own 128 columns; otherwise
+          // every pass adds into the same accumulator.
+          const int pass = MODE == MODE_WGRAD ? 0 : kb / kb_pass;
+          const int kin = MODE == MODE_WGRAD ? kb : kb - pass * kb_pass;
+          const uint32_t d_tmem = d0 + (MODE == MODE_DSWIGLU ? static_cast<uint32_t>(pass * BNH) : 0u);
+          const bool first = MODE == MODE_DX ? (kb == 0) : (kin == 0);
+          const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            ptx::umma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2),
+                           ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2), S::idesc, (first && kk == 0) ? 0u : 1u);
+          }
+          ptx::umma_commit(&ctl->empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (nkb > 0) {
+          ptx::umma_commit(&ctl->tfull[acc]);
+        } else {
+          ptx::mbar_arrive(&ctl->tfull[acc]);  // nothing to wait for: the epilogue writes zeros
+        }
+        if (++acc == S::n_acc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      ptx::umma_commit(&ctl->drain);
+      ptx::mbar_wait(&ctl->drain, 0, nullptr, drain_limit(args.wait_ns));
+    }
+  } else {
+    // -------------------------------------------------- epilogue (warps 2-5)
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int e, m, n;
+      decode_tile(ctl, args.E, tile, e, m, n);
+      const bool ready = ptx::mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag, args.wait_ns);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+        raise_abort(ctl, args.status);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * S::acc_cols);
+      if (MODE == MODE_DSWIGLU) {
+        const int grow = ctl->seg[e] + m * BM + row_in_tile;
+        const bool row_ok = grow < ctl->seg[e + 1];
+        const int col0 = n * BNH;
+        const float wp = row_ok ? __ldg(args.w_perm + grow) : 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < BNH; c += 32) {
+          uint32_t dh[32], av[32], bv[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c, dh);
+          ptx::tmem_ld_32x32b_x32(t_row + BNH + c, av);
+          ptx::tmem_ld_32x32b_x32(t_row + 2 * BNH + c, bv);
+          ptx::tmem_ld_wait();
+          if (row_ok && col0 + c < args.n_out) {
+            uint32_t pa[16], pb[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float da[2], db[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float g = wp * __uint_as_float(dh[2 * i + h]);
+                const float a = __uint_as_float(av[2 * i + h]);
+                const float b = __uint_as_float(bv[2 * i + h]);
+                const float s = 1.0f / (1.0f + __expf(-a));
+                const float silu = a * s;
+                da[h] = g * b * (s * (1.0f + a * (1.0f - s)));
+                db[h] = g * silu;
+              }
+              pa[i] = pack_bf16x2(da[0], da[1]);
+              pb[i] = pack_bf16x2(db[0], db[1]);
+            }
+            uint4* dA = reinterpret_cast<uint4*>(args.out0 + static_cast<size_t>(grow) * args.n_out + col0 + c);
+            uint4* dB = reinterpret_cast<uint4*>(args.out1 + static_cast<size_t>(grow) * args.n_out + col0 + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              dA[q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+              dB[q] = make_uint4(pb[4 * q], pb[4 * q + 1], pb[4 * q + 2], pb[4 * q + 3]);
+            }
+          }
+        }
+      } else if (MODE == MODE_DX) {
+        const int grow = ctl->seg[e] + m * BM + row_in_tile;
+        const bool row_ok = grow < ctl->seg[e + 1];
+        const int col0 = n * 2 * BNH;
+#pragma unroll 1
+        for (int c = 0; c < 2 * BNH; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c, v);
+          ptx::tmem_ld_wait();
+          if (row_ok && col0 + c < args.n_out) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            uint4* dst = reinterpret_cast<uint4*>(args.out0 + static_cast<size_t>(grow) * args.n_out + col0 + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      } else {
+        // WGRAD: row m*128 + r of expert e's [M, N] fp32 gradient.
+        const int row = m * BM + row_in_tile;
+        const bool row_ok = row < args.m_rows;
+        const bool empty = ctl->rows[e] == 0;
+        const int col0 = n * 2 * BNH;
+        float* base = args.outf + (static_cast<size_t>(e) * args.m_rows + row) * args.n_out;
+#pragma unroll 1
+        for (int c = 0; c < 2 * BNH; c += 32) {
+          uint32_t v[32];
+          if (!empty) {
+            ptx::tmem_ld_32x32b_x32(t_row + c, v);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+          if (row_ok && col0 + c < args.n_out) {
+            float4* dst = reinterpret_cast<float4*>(base + col0 + c);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ctl->tempty[acc]);
+      if (++acc == S::n_acc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_dealloc(tmem_base, S::tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+  });
+  return fn;
+}
+
+// Row-major bf16 [rows, inner] -> 64 x 128 boxes, 128-byte swizzle, zero fill.
+int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return MOE_ECUDA;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {BK, BNH};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
+}
+
+template <int MODE>
+int smem_attr_once(int device) {
+  static std::mutex mu;
+  static bool done[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) return MOE_ECUDA;
+  if (!done[device]) {
+    if (cudaFuncSetAttribute(bwd_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+      return MOE_ECUDA;
+    done[device] = true;
+  }
+  return MOE_OK;
+}
+
+template <int MODE>
+int launch_bwd(const Maps& maps, BwdArgs a, long long max_tiles, const Ctx& c, cudaStream_t s) {
+  int rc = smem_attr_once<MODE>(c.device);
+  if (rc != MOE_OK) return rc;
+  a.status = c.status;
+  a.wait_ns = c.wait_ns;
+  long long grid = max_tiles < c.num_sms ? max_tiles : c.num_sms;
+  if (grid < 1) grid = 1;
+  launch_pdl(bwd_gemm_kernel<MODE>, static_cast<int>(grid), THREADS, SMEM_BYTES, s, maps, a);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
+
+}  // namespace
+
+// Columns of the [channels, padded tokens] layout: every expert's tokens
+// padded to a multiple of 64, rounded up to a multiple of 64 so that the row
+// stride is a multiple of 128 bytes (a tensor map needs multiples of 16).
+size_t bwd_kpad_cols(int Tk, int E) {
+  const size_t cols = static_cast<size_t>(Tk) + static_cast<size_t>(E) * KPAD;
+  return (cols + KPAD - 1) / KPAD * KPAD;
+}
+
+int launch_bwd_dswiglu(const void* dout_perm, const float* w_perm, const void* x_perm, const int32_t* offsets,
+                       const void* W2t, const void* W1, const void* W3, void* dA, void* dB, int Tk, int d, int dff,
+                       int E, const Ctx& c, cudaStream_t s) {
+  if (Tk <= 0) return MOE_OK;
+  Maps m;
+  int rc = make_tmap(&m.a[0], dout_perm, d, Tk);
+  if (rc == MOE_OK) rc = make_tmap(&m.a[1], x_perm, d, Tk);
+  if (rc == MOE_OK) m.a[2] = m.a[1];
+  if (rc == MOE_OK) rc = make_tmap(&m.b[0], W2t, d, static_cast<uint64_t>(E) * dff);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[1], W1, d, static_cast<uint64_t>(E) * dff);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[2], W3, d, static_cast<uint64_t>(E) * dff);
+  if (rc != MOE_OK) return rc;
+  BwdArgs a = {};
+  a.offsets = offsets;
+  a.E = E;
+  a.Tk = Tk;
+  a.K = d;
+  a.b_rows = dff;
+  a.n_out = dff;
+  a.n_tiles = (dff + BNH - 1) / BNH;
+  a.out0 = static_cast<__nv_bfloat16*>(dA);
+  a.out1 = static_cast<__nv_bfloat16*>(dB);
+  a.w_perm = w_perm;
+  const long long max_tiles = (static_cast<long long>(Tk) / BM + (E < Tk ? E : Tk)) * a.n_tiles;
+  return launch_bwd<MODE_DSWIGLU>(m, a, max_tiles, c, s);
+}
+
+int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const void* W1t, const void* W3t,
+                  void* dx_perm, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s) {
+  if (Tk <= 0) return MOE_OK;
+  Maps m;
+  int rc = make_tmap(&m.a[0], dA, dff, Tk);
+  if (rc == MOE_OK) rc = make_tmap(&m.a[1], dB, dff, Tk);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[0], W1t, dff, static_cast<uint64_t>(E) * d);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[1], W3t, dff, static_cast<uint64_t>(E) * d);
+  if (rc != MOE_OK) return rc;
+  m.a[2] = m.a[1];
+  m.b[2] = m.b[1];
+  BwdArgs a = {};
+  a.offsets = offsets;
+  a.E = E;
+  a.Tk = Tk;
+  a.K = dff;
+  a.b_rows = d;
+  a.n_out = d;
+  a.n_tiles = (d + 2 * BNH - 1) / (2 * BNH);
+  a.out0 = static_cast<__nv_bfloat16*>(dx_perm);
+  const long long max_tiles = (static_cast<long long>(Tk) / BM + (E < Tk ? E : Tk)) * a.n_tiles;
+  return launch_bwd<MODE_DX>(m, a, max_tiles, c, s);
+}
+
+int launch_bwd_wgrad(const void* At, const void* Bt, const int32_t* offsets, float* dW, int M, int N, int Tk, int E,
+                     const Ctx& c, cudaStream_t s) {
+  Maps m;
+  const uint64_t kp = bwd_kpad_cols(Tk, E);
+  int rc = make_tmap(&m.a[0], At, kp, static_cast<uint64_t>(M));
+  if (rc == MOE_OK) rc = make_tmap(&m.b[0], Bt, kp, static_cast<uint64_t>(N));
+  if (rc != MOE_OK) return rc;
+  m.a[1] = m.a[2] = m.a[0];
+  m.b[1] = m.b[2] = m.b[0];
+  BwdArgs a = {};
+  a.offsets = offsets;
+  a.E = E;
+  a.Tk = Tk;
+  a.K = 0;
+  a.b_rows = 0;
+  a.n_out = N;
+  a.m_rows = M;
+  a.n_tiles = (N + 2 * BNH - 1) / (2 * BNH);
+  a.outf = dW;
+  const long long max_tiles = static_cast<long long>(E) * ((M + BM - 1) / BM) * a.n_tiles;
+  return launch_bwd<MODE_WGRAD>(m, a, max_tiles, c, s);
+}
+
+}  // namespace moe

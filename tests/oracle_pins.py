@@ -551,6 +551,17 @@ def pin_backward_silu_derivative(o):
     assert abs(o.silu_grad(np.array([-40.0]))[0]) < 1e-12
 
 
+def pin_backward_scale_bounds_gradient(o):
+    """The sum of absolute terms bounds each gradient element (triangle
+    inequality) and is zero exactly where no term contributes."""
+    L = _tiny_layer(97, T=10, d=8, F=6, E=4)
+    g = o.moe_backward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], 2, _rng(98).standard_normal((10, 8)),
+                       with_scale=True)
+    for n in ("dx", "dWg", "dW1", "dW3", "dW2"):
+        assert np.all(np.abs(g[n]) <= g[n + "_scale"] * (1 + 1e-12) + 1e-300), n
+        assert np.all(g[n][g[n + "_scale"] == 0] == 0), n
+
+
 def pin_backward_linear_in_dout(o):
     """The gradients are linear in the output gradient."""
     L = _tiny_layer(93, T=12, d=8, F=6, E=4)

@@ -125,3 +125,25 @@ def check_close(got, ref, dtype: str, what: str):
 
 def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().to(torch.float64).numpy() if t.is_floating_point() else t.detach().cpu().numpy()
+
+
+def check_backward_close(got, ref, scale, what, c=2.0 ** -7):
+    """Gradient parity: relative L2 within the bf16 bound, and every element
+    within c times its sum of absolute terms (``scale``, from the oracle).
+
+    The first-order rounding-error bound of a sum of products whose factors
+    were each rounded to bf16 (relative error u = 2^-9) and accumulated in
+    fp32 over n terms is (2u + n 2^-24) times the sum of the absolute terms;
+    c = 2^-7 covers two rounded factors per term and fp32 accumulation over
+    up to ~16K terms (2^-8 + 2^-10)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    r = rel_l2(got, ref)
+    assert r <= REL_L2["bf16"], f"{what}: rel-L2 {r:.3e} > {REL_L2['bf16']}"
+    err = np.abs(got - ref)
+    bound = c * np.asarray(scale, dtype=np.float64) + 1e-30
+    worst = float(np.max(err / bound))
+    assert worst <= 1.0, f"{what}: an element is off by {worst:.2f}x its rounding-error bound"
+    return r, worst

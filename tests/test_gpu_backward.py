@@ -1,0 +1,122 @@
+"""Parity of the backward (Mixtral 8x7B model reference page, Training:
+experts and router trained together) through the C ABI with the fp64 oracle's
+gradients, on GPU.
+
+The forward runs with caller scratch (moe_forward_ws); that scratch is the
+backward's `saved` input.  dout is a seeded normal in bf16.  The oracle
+differentiates with the GPU's routing wherever the forward's routing was a
+near tie.  Gradients are compared by relative L2 (bf16 tolerance, 5e-3) and
+a per-element bound; an expert with no tokens must get exactly zero weight
+gradients.
+
+Per-element bound (parity.check_backward_close): 2^-7 times the element's
+sum of absolute terms through the chain, from the oracle - the first-order
+bound of sums of products of bf16-rounded factors (the forward's h and y;
+the backward's dy, da, db and permuted dx) accumulated in fp32.  The
+gradients are sums in which terms can cancel, so neither the element nor its
+row's RMS bounds their rounding error; a wrong row or tile breaks this bound
+by orders of magnitude.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_workloads as mw
+import oracle.moe_oracle as O
+from parity import check_backward_close, check_routing, effective_routing, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from sparse_mixture_experts_50_b300 import binding
+    binding.lib()
+    binding.moe_get_device_status(reset=True)
+    return binding
+
+
+def status_ok(B):
+    s = B.moe_get_device_status(reset=True)
+    assert s == 0, f"device status {s}"
+
+
+def seeded_dout(T, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((T, d), generator=g).to(torch.bfloat16)
+
+
+def run_gpu(B, t, k, dout, entry="alloc"):
+    g = {n: v.to(DEV).contiguous() for n, v in t.items()}
+    T, d = g["x"].shape
+    E, F, _ = g["W1"].shape
+    saved = B.workspace(T, d, F, E, k, B.MOE_DTYPE_BF16)
+    B.moe_forward_ws(g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved)
+    dd = dout.to(DEV)
+    if entry == "ws":
+        ws = torch.empty(B.moe_backward_workspace_bytes(T, d, F, E, k), dtype=torch.uint8, device=DEV)
+        grads = B.moe_backward_ws(dd, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved, ws)
+    else:
+        grads = B.moe_backward(dd, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved)
+    status_ok(B)
+    idx = saved[: T * k * 4].view(torch.int32).reshape(T, k).cpu().numpy()
+    w = saved[256 * ((T * k * 4 + 255) // 256):][: T * k * 4].view(torch.float32).reshape(T, k).cpu().numpy()
+    return grads, idx, w
+
+
+def oracle_grads(t, k, dout, gidx, gw, experts=None):
+    ora_w, ora_idx, logits = O.router(t["x"], t["Wg"], k)
+    check_routing(gidx, gw, ora_idx, ora_w, logits, k)
+    _, idx_eff = effective_routing(gidx, ora_w, ora_idx, logits)
+    return O.moe_backward(t["x"], t["Wg"], t["W1"], t["W3"], t["W2"], k, dout, idx=idx_eff, experts=experts,
+                          with_scale=True), idx_eff
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "small_ragged", "small_skewed_zero"])
+@pytest.mark.parametrize("entry", ["alloc", "ws"])
+def test_backward_small(B, name, entry):
+    wl = mw.get(name)
+    t = mw.make_inputs(wl)
+    dout = seeded_dout(wl.T, wl.d, 7)
+    grads, gidx, gw = run_gpu(B, t, wl.k, dout, entry)
+    ref, idx_eff = oracle_grads(t, wl.k, dout, gidx, gw)
+    for n in ("dx", "dWg", "dW1", "dW3", "dW2"):
+        check_backward_close(to_np(grads[n]), ref[n], ref[n + "_scale"], f"{name} {n}")
+    used = set(np.unique(idx_eff).tolist())
+    for e in range(wl.E):
+        if e not in used:
+            for n in ("dW1", "dW3", "dW2"):
+                assert torch.count_nonzero(grads[n][e]).item() == 0, f"{name}: unused expert {e} has {n} != 0"
+
+
+def test_backward_linear_in_dout(B):
+    """Scaling dout by 2 scales every gradient by exactly 2 (every rounding
+    step commutes with a power of two), so the GPU gradients are linear and
+    deterministic."""
+    wl = mw.get("small_bf16")
+    t = mw.make_inputs(wl)
+    dout = seeded_dout(wl.T, wl.d, 8)
+    g1, _, _ = run_gpu(B, t, wl.k, dout)
+    g2, _, _ = run_gpu(B, t, wl.k, dout * 2)
+    for n in g1:
+        assert torch.equal(g2[n], 2 * g1[n]), n
+
+
+def test_backward_mixtral_shape(B):
+    """Mixtral sizes (d=4096, d_ff=14336, E=8, top-2) at 64 tokens: dx and dWg
+    in full, the expert weight gradients of two experts."""
+    wl = mw.get("decode").with_tokens(64)
+    t = mw.make_inputs(wl)
+    dout = seeded_dout(wl.T, wl.d, 9)
+    grads, gidx, gw = run_gpu(B, t, wl.k, dout)
+    counts = np.bincount(gidx.ravel(), minlength=wl.E)
+    pick = [int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))]
+    ref, _ = oracle_grads(t, wl.k, dout, gidx, gw, experts=pick)
+    for n in ("dx", "dWg"):
+        check_backward_close(to_np(grads[n]), ref[n], ref[n + "_scale"], f"mixtral {n}")
+    for e in pick:
+        for n in ("dW1", "dW3", "dW2"):
+            check_backward_close(to_np(grads[n][e]), ref[n][e], ref[n + "_scale"][e], f"mixtral {n}[{e}]")
