@@ -46,7 +46,7 @@ import moe_workloads as mw  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (Mixtral 4096/14336, E8 k2, bf16) + % of roofline"
 HEADLINE = "decode"
-ALL_BENCH = ["decode", "prefill", "skewed", "skewed_zero", "block", "decode_w8", "prefill_w8"]
+ALL_BENCH = ["decode", "prefill", "skewed", "skewed_zero", "block", "decode_w8", "prefill_w8", "prefill_bwd"]
 L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = {False: 6, True: 7}  # router, rank, gather, gate_up, down, combine (+ rmsnorm)
 
@@ -232,13 +232,41 @@ class Layer:
         return self.out
 
 
+class BwdLayer:
+    """The backward of one workload: the forward runs once at set-up with
+    caller scratch (`saved`), then step() runs moe_backward_ws through the C
+    ABI into preallocated gradients."""
+
+    def __init__(self, wl, tensors, device):
+        from sparse_mixture_experts_50_b300 import binding as B
+        self.B = B
+        self.wl = wl
+        T, d, F, E, k = wl.T, wl.d, wl.F, wl.E, wl.k
+        g = {n: v.to(device) for n, v in tensors.items()}
+        self.x, self.Wg, self.W1, self.W3, self.W2, self.dout = g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], g["dout"]
+        self.saved = B.workspace(T, d, F, E, k, B.MOE_DTYPE_BF16, device=device)
+        B.moe_forward_ws(self.x, self.Wg, self.W1, self.W3, self.W2, k, self.saved)
+        self.ws = torch.empty(B.moe_backward_workspace_bytes(T, d, F, E, k), dtype=torch.uint8, device=device)
+        self.grads = B._grads(self.x, self.Wg, self.W1, self.W3, self.W2, None)
+
+    def step(self, ev=None):
+        if ev is not None:
+            ev[0].record()
+        self.B.moe_backward_ws(self.dout, self.x, self.Wg, self.W1, self.W3, self.W2, self.wl.k, self.saved, self.ws,
+                               self.grads)
+        if ev is not None:
+            for e in ev[1:]:
+                e.record()
+        return self.grads
+
+
 def make_tensors(wl, shared):
     """CPU tensors of a workload; the expert weights (which do not depend on
     T or the gate bias) are drawn once and shared across workloads."""
     key = (wl.d, wl.F, wl.E, wl.dtype, wl.init)
     if key not in shared:
         shared[key] = mw.make_inputs(wl, only=("W1", "W3", "W2"))
-    rest = mw.make_inputs(wl, only=("x", "Wg", "gamma"))
+    rest = mw.make_inputs(wl, only=("x", "Wg", "gamma", "dout"))
     return {**rest, **shared[key]}
 
 
@@ -270,8 +298,39 @@ def time_layer(layer, steps, warmup, flush, dist_on):
     return step_ms, parts, wall
 
 
+def bench_backward(name, shared, args, device, peaks, dist_on):
+    """The backward leg: T / (mean backward time); its tensor roofline uses
+    the algorithmic 12*d*F FLOP per routed row (dh 2, dx 4, dW2 2, dW1+dW3 4;
+    the recomputation of a and b is implementation work and not counted)."""
+    wl = mw.get(name)
+    layer = BwdLayer(wl, make_tensors(wl, shared), device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    layer.step()
+    status = layer.B.moe_get_device_status(reset=True)
+    if status != 0:
+        raise RuntimeError(f"{name}: device status {status} after the first step")
+    step_ms, _, wall = time_layer(layer, args.steps, args.warmup, flush, dist_on)
+    status = layer.B.moe_get_device_status(reset=True)
+    if status != 0:
+        raise RuntimeError(f"{name}: device status {status} after the timed steps")
+    ms = sum(step_ms) / len(step_ms)
+    flops = wl.T * wl.k * 12 * wl.d * wl.F + wl.T * wl.k * 4 * wl.d * wl.E
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {
+        "workload": name, "T": wl.T, "tokens_per_s": wl.T / (ms * 1e-3), "ms_per_step": ms,
+        "layer_roofline_frac": achieved / peaks["bf16_tflops"], "bound": "tensor",
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "kernel": "whole backward (moe_backward_ws)", "algorithmic_per_launch": flops, "traffic": None},
+        "wall_s": wall,
+    }, layer
+
+
 def bench_workload(name, shared, args, device, peaks, dist_on):
     wl = mw.get(name)
+    if wl.bwd:
+        return bench_backward(name, shared, args, device, peaks, dist_on)
     layer = Layer(wl, make_tensors(wl, shared), device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     layer.step()
@@ -398,7 +457,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workloads", default=",".join(ALL_BENCH))
-    ap.add_argument("--headline", default=HEADLINE, choices=[n for n in ALL_BENCH if not mw.get(n).w8],
+    ap.add_argument("--headline", default=HEADLINE, choices=[n for n in ALL_BENCH if not (mw.get(n).w8 or mw.get(n).bwd)],
                     help="workload of the JSON line's value (default: Mixtral-shape decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -47,7 +47,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 SKEW_BIAS_FILE = os.path.join(_HERE, "skew_bias.json")
 
 # One generator stream per tensor.
-_STREAM = {"x": 1, "Wg": 2, "W1": 3, "W3": 4, "W2": 5, "gamma": 6}
+_STREAM = {"x": 1, "Wg": 2, "W1": 3, "W3": 4, "W2": 5, "gamma": 6, "dout": 7}
 
 
 @dataclass(frozen=True)
@@ -67,6 +67,7 @@ class Workload:
     eps: float = RMSNORM_EPS
     bias_key: str | None = None  # skew_bias.json entry (default: name)
     w8: bool = False  # expert weights quantised to int8 (per-row scales) before use
+    bwd: bool = False  # the backward of the layer (dout drawn from stream "dout")
 
     @property
     def Tk(self) -> int:
@@ -97,6 +98,9 @@ WORKLOADS = {
     # here are quantised per row before the layer runs.
     "decode_w8": _mixtral("decode_w8", 16, w8=True),
     "prefill_w8": _mixtral("prefill_w8", 4096, w8=True),
+    # The backward of the prefill batch (Mixtral 8x7B model reference page,
+    # Training): dout ~ N(0, 1) in bf16.
+    "prefill_bwd": _mixtral("prefill_bwd", 4096, bwd=True),
 }
 
 # Reduced sizes with the same structure, small enough for the oracle to finish
@@ -176,6 +180,8 @@ def make_inputs(wl: Workload, seed: int = 0, bias: list[float] | None = None,
     }
     if wl.block:
         recipe["gamma"] = lambda: 1.0 + _normal((d,), 0.02, seed, "gamma")
+    if wl.bwd:
+        recipe["dout"] = lambda: _normal((T, d), 1.0, xs, "dout")
     names = list(recipe) if only is None else [n for n in recipe if n in only]
     out = {n: recipe[n]() for n in names}
     if wl.skew is not None:

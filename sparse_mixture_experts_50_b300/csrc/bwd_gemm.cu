@@ -16,9 +16,10 @@
 // transposed to [channels, tokens] with each expert's tokens padded to a
 // multiple of 64 (zeros), so that every K step of an expert starts on a
 // 128-byte boundary.
-//   DSWIGLU  tile 128 rows x 128 h columns; three K=d passes accumulate
-//            dout W2, a and b into three 128-column accumulators (tensor
-//            memory columns 0-383); the epilogue scales the first by w_p in
+//   DSWIGLU  tile 128 rows x 128 h columns; two K=d passes: dout W2 (N=128)
+//            into columns 0-127, then a and b together (N=256, the W1 rows
+//            then the W3 rows of the tile's columns, as in the forward's
+//            gate/up GEMM) into columns 128-383; the epilogue scales the first by w_p in
 //            fp32 (dout is gathered exactly, so dh is not exposed to a bf16
 //            rounding of w dout, which its 4096-term sum can amplify where
 //            it cancels), forms da, db in fp32 and rounds them to bf16.  a
@@ -29,6 +30,9 @@
 //   WGRAD    per expert an [M, N] fp32 matrix, tile 128 x 256, K = the
 //            expert's padded token segment; an expert with no tokens gets
 //            zeros (its tiles skip the MMAs).
+// Epilogue stores go through a per-warp 32 x 32 staging block in shared
+// memory, so that each store instruction writes contiguous row segments
+// (a lane per row would make every instruction touch 32 rows).
 // Every wait is bounded as in the forward kernel.
 #include <cuda.h>
 #include <mutex>
@@ -68,7 +72,11 @@ struct Ctl {
   int rows[MAX_E];       // WGRAD: real tokens of each expert
 };
 
-constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(Ctl);
+constexpr int STG_PITCH = 33;             // staging block row pitch (32-bit words)
+constexpr int STG_WORDS = 32 * STG_PITCH;  // one warp's staging block
+constexpr size_t CTL_BYTES = (sizeof(Ctl) + 15) / 16 * 16;
+constexpr size_t SMEM_BYTES =
+    1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + CTL_BYTES + 4 * STG_WORDS * sizeof(uint32_t);
 
 struct BwdArgs {
   const int32_t* offsets;  // [E+1] routed-row boundaries
@@ -110,15 +118,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The warp's 32 rows x 32 fp32 columns (lane = row, v[i] = column i) to
+// dst[r * ld + i] for r < rows: one coalesced 128-byte row per instruction.
+__device__ __forceinline__ void warp_store_f32(uint32_t* stg, const uint32_t (&v)[32], float* dst, size_t ld,
+                                               int rows, int lane) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) stg[lane * STG_PITCH + i] = v[i];
+  __syncwarp();
+  for (int r = 0; r < rows; ++r) dst[r * ld + lane] = __uint_as_float(stg[r * STG_PITCH + lane]);
+  __syncwarp();
+}
+
+// The warp's 32 rows x 32 bf16 columns (lane = row, pk[i] = columns 2i,
+// 2i+1) to dst[r * ld + ...] for r < rows: two 64-byte rows per instruction.
+__device__ __forceinline__ void warp_store_bf16(uint32_t* stg, const uint32_t (&pk)[16], __nv_bfloat16* dst,
+                                                size_t ld, int rows, int lane) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) stg[lane * 17 + i] = pk[i];
+  __syncwarp();
+  const int half = lane >> 4, w = lane & 15;
+  for (int r = half; r < rows; r += 2)
+    reinterpret_cast<uint32_t*>(dst + r * ld)[w] = stg[r * 17 + w];
+  __syncwarp();
+}
+
 template <int MODE>
 struct Shape {
-  static constexpr int passes = MODE == MODE_DSWIGLU ? 3 : (MODE == MODE_DX ? 2 : 1);
+  static constexpr int passes = MODE == MODE_DSWIGLU ? 2 : (MODE == MODE_DX ? 2 : 1);
   static constexpr int n_tile = MODE == MODE_DSWIGLU ? BNH : 2 * BNH;   // output columns per tile
   static constexpr int b_boxes = MODE == MODE_DSWIGLU ? 1 : 2;
   static constexpr int acc_cols = MODE == MODE_DSWIGLU ? 3 * BNH : 2 * BNH;
   static constexpr int n_acc = MODE == MODE_DSWIGLU ? 1 : 2;             // accumulators in flight
   static constexpr int tmem_cols = 512;
   static constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, b_boxes * BNH);
+  static constexpr uint32_t idesc_wide = ptx::idesc_bf16_f32(BM, 2 * BNH);  // DSWIGLU pass 1
 };
 
 // Tensor maps per pass: A (token rows or, WGRAD, channel rows) and B.
@@ -133,6 +166,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* stage_blocks = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES + CTL_BYTES);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const volatile int* abort_flag = &ctl->abort_flag;
@@ -151,7 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int p = 0; p < S::passes; ++p) {
+    for (int p = 0; p < 3; ++p) {
       ptx::prefetch_tmap(&maps.a[p]);
       ptx::prefetch_tmap(&maps.b[p]);
     }
@@ -238,12 +272,19 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
             brow = e * args.b_rows + n * S::n_tile;
           }
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          constexpr int bytes = A_BYTES + S::b_boxes * BNH * BK * 2;
+          // DSWIGLU pass 1 stages two B boxes from two tensors (W1, W3) at
+          // the same rows; DX and WGRAD two consecutive 128-row boxes.
+          const bool wide = MODE == MODE_DSWIGLU ? pass == 1 : S::b_boxes == 2;
+          const int bytes = A_BYTES + (wide ? 2 : 1) * BNH * BK * 2;
           ptx::mbar_arrive_expect_tx(&ctl->full[stage], bytes);
           ptx::tma_load_2d(sa, &maps.a[pass], &ctl->full[stage], kx, arow);
           ptx::tma_load_2d(sa + A_BYTES, &maps.b[pass], &ctl->full[stage], kx, brow);
-          if (S::b_boxes == 2)
-            ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[pass], &ctl->full[stage], kx, brow + BNH);
+          if (wide) {
+            if (MODE == MODE_DSWIGLU)
+              ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[2], &ctl->full[stage], kx, brow);
+            else
+              ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[pass], &ctl->full[stage], kx, brow + BNH);
+          }
           filled |= 1u << stage;
           last_parity[stage] = phase;
           if (++stage == STAGES) {
@@ -281,18 +322,19 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
             break;
           }
           ptx::tc_fence_after();
-          // DSWIGLU: pass p accumulates into its own 128 columns; otherwise
-          // every pass adds into the same accumulator.
+          // DSWIGLU: pass 0 (N=128) into columns 0-127, pass 1 (N=256) into
+          // 128-383; otherwise every pass adds into the same accumulator.
           const int pass = MODE == MODE_WGRAD ? 0 : kb / kb_pass;
           const int kin = MODE == MODE_WGRAD ? kb : kb - pass * kb_pass;
           const uint32_t d_tmem = d0 + (MODE == MODE_DSWIGLU ? static_cast<uint32_t>(pass * BNH) : 0u);
+          const uint32_t idesc = (MODE == MODE_DSWIGLU && pass == 1) ? S::idesc_wide : S::idesc;
           const bool first = MODE == MODE_DX ? (kb == 0) : (kin == 0);
           const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             ptx::umma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2),
-                           ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2), S::idesc, (first && kk == 0) ? 0u : 1u);
+                           ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2), idesc, (first && kk == 0) ? 0u : 1u);
           }
           ptx::umma_commit(&ctl->empty[stage]);
           if (++stage == STAGES) {
@@ -317,7 +359,6 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
   } else {
     // -------------------------------------------------- epilogue (warps 2-5)
     const int quad = warp & 3;
-    const int row_in_tile = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -331,11 +372,13 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
       ptx::tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * S::acc_cols);
+      uint32_t* stg = stage_blocks + quad * STG_WORDS;
       if (MODE == MODE_DSWIGLU) {
-        const int grow = ctl->seg[e] + m * BM + row_in_tile;
-        const bool row_ok = grow < ctl->seg[e + 1];
+        const int row0 = ctl->seg[e] + m * BM + quad * 32;  // the warp's first row
+        const int rows = max(0, min(32, ctl->seg[e + 1] - row0));
+        const bool row_ok = lane < rows;
         const int col0 = n * BNH;
-        const float wp = row_ok ? __ldg(args.w_perm + grow) : 0.0f;
+        const float wp = row_ok ? __ldg(args.w_perm + row0 + lane) : 0.0f;
 #pragma unroll 1
         for (int c = 0; c < BNH; c += 32) {
           uint32_t dh[32], av[32], bv[32];
@@ -343,7 +386,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
           ptx::tmem_ld_32x32b_x32(t_row + BNH + c, av);
           ptx::tmem_ld_32x32b_x32(t_row + 2 * BNH + c, bv);
           ptx::tmem_ld_wait();
-          if (row_ok && col0 + c < args.n_out) {
+          if (rows > 0 && col0 + c < args.n_out) {
             uint32_t pa[16], pb[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -361,40 +404,35 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
               pa[i] = pack_bf16x2(da[0], da[1]);
               pb[i] = pack_bf16x2(db[0], db[1]);
             }
-            uint4* dA = reinterpret_cast<uint4*>(args.out0 + static_cast<size_t>(grow) * args.n_out + col0 + c);
-            uint4* dB = reinterpret_cast<uint4*>(args.out1 + static_cast<size_t>(grow) * args.n_out + col0 + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              dA[q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
-              dB[q] = make_uint4(pb[4 * q], pb[4 * q + 1], pb[4 * q + 2], pb[4 * q + 3]);
-            }
+            const size_t base = static_cast<size_t>(row0) * args.n_out + col0 + c;
+            warp_store_bf16(stg, pa, args.out0 + base, args.n_out, rows, lane);
+            warp_store_bf16(stg, pb, args.out1 + base, args.n_out, rows, lane);
           }
         }
       } else if (MODE == MODE_DX) {
-        const int grow = ctl->seg[e] + m * BM + row_in_tile;
-        const bool row_ok = grow < ctl->seg[e + 1];
+        const int row0 = ctl->seg[e] + m * BM + quad * 32;
+        const int rows = max(0, min(32, ctl->seg[e + 1] - row0));
         const int col0 = n * 2 * BNH;
 #pragma unroll 1
         for (int c = 0; c < 2 * BNH; c += 32) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c, v);
           ptx::tmem_ld_wait();
-          if (row_ok && col0 + c < args.n_out) {
+          if (rows > 0 && col0 + c < args.n_out) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(args.out0 + static_cast<size_t>(grow) * args.n_out + col0 + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            warp_store_bf16(stg, pk, args.out0 + static_cast<size_t>(row0) * args.n_out + col0 + c, args.n_out, rows,
+                            lane);
           }
         }
       } else {
-        // WGRAD: row m*128 + r of expert e's [M, N] fp32 gradient.
-        const int row = m * BM + row_in_tile;
-        const bool row_ok = row < args.m_rows;
+        // WGRAD: rows m*128 + quad*32 .. of expert e's [M, N] fp32 gradient.
+        const int row0 = m * BM + quad * 32;
+        const int rows = max(0, min(32, args.m_rows - row0));
         const bool empty = ctl->rows[e] == 0;
         const int col0 = n * 2 * BNH;
-        float* base = args.outf + (static_cast<size_t>(e) * args.m_rows + row) * args.n_out;
+        float* base = args.outf + (static_cast<size_t>(e) * args.m_rows + row0) * args.n_out;
 #pragma unroll 1
         for (int c = 0; c < 2 * BNH; c += 32) {
           uint32_t v[32];
@@ -405,13 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
           }
-          if (row_ok && col0 + c < args.n_out) {
-            float4* dst = reinterpret_cast<float4*>(base + col0 + c);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-          }
+          if (rows > 0 && col0 + c < args.n_out) warp_store_f32(stg, v, base + col0 + c, args.n_out, rows, lane);
         }
       }
       ptx::tc_fence_before();
@@ -509,7 +541,7 @@ int launch_bwd_dswiglu(const void* dout_perm, const float* w_perm, const void* x
   Maps m;
   int rc = make_tmap(&m.a[0], dout_perm, d, Tk);
   if (rc == MOE_OK) rc = make_tmap(&m.a[1], x_perm, d, Tk);
-  if (rc == MOE_OK) m.a[2] = m.a[1];
+  if (rc == MOE_OK) m.a[2] = m.a[1];  // unused
   if (rc == MOE_OK) rc = make_tmap(&m.b[0], W2t, d, static_cast<uint64_t>(E) * dff);
   if (rc == MOE_OK) rc = make_tmap(&m.b[1], W1, d, static_cast<uint64_t>(E) * dff);
   if (rc == MOE_OK) rc = make_tmap(&m.b[2], W3, d, static_cast<uint64_t>(E) * dff);

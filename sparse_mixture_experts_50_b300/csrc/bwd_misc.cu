@@ -160,36 +160,67 @@ __global__ void __launch_bounds__(256) dwg_reduce_kernel(const float* __restrict
 }
 
 // ---------------------------------------------------------------- transposes
-// [B, R, C] -> [B, C, R], 64 x 64 tiles through shared memory.
+// 64 x 64 tiles through shared memory with 16-byte global accesses: each
+// thread loads 8 consecutive columns of a source row, and writes 8
+// consecutive rows of one column as a 16-byte run of a destination row
+// (a warp's lanes take 32 consecutive columns, so its shared-memory reads of
+// one row are conflict-free).
+constexpr int kTp = 72;  // tile row pitch in elements (144 bytes, 16-byte aligned)
+
+__device__ __forceinline__ void tile_store_out(const __nv_bfloat16 (*tile)[kTp], __nv_bfloat16* dst_row, int col,
+                                               int r0, int rows_ok) {
+  // dst_row points at destination row `col`; writes rows r0 .. r0+7 of the tile's column.
+  uint32_t w[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint16_t lo = __bfloat16_as_ushort(tile[r0 + 2 * m][col]);
+    const uint16_t hi = __bfloat16_as_ushort(tile[r0 + 2 * m + 1][col]);
+    w[m] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  if (rows_ok >= 8) {
+    *reinterpret_cast<uint4*>(dst_row) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    for (int m = 0; m < rows_ok; ++m)
+      dst_row[m] = __ushort_as_bfloat16(static_cast<uint16_t>(w[m >> 1] >> (16 * (m & 1))));
+  }
+}
+
+// [B, R, C] -> [B, C, R].  C % 8 == 0 and R % 8 == 0.
 __global__ void __launch_bounds__(256) transpose_batched_kernel(const __nv_bfloat16* __restrict__ src,
                                                                 __nv_bfloat16* __restrict__ dst, int R, int C) {
-  __shared__ __nv_bfloat16 tile[64][66];
+  __shared__ __align__(16) __nv_bfloat16 tile[64][kTp];
   pdl_enter();
   const size_t b = blockIdx.z;
   const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
   const __nv_bfloat16* s = src + b * R * C;
   __nv_bfloat16* o = dst + b * R * C;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
-  for (int r = ty; r < 64; r += 4) {
-    const int gr = r0 + r, gc = c0 + tx;
-    tile[r][tx] = (gr < R && gc < C) ? s[static_cast<size_t>(gr) * C + gc] : __float2bfloat16(0.0f);
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int r = i >> 3, q = (i & 7) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + r < R && c0 + q < C) v = __ldg(reinterpret_cast<const uint4*>(s + static_cast<size_t>(r0 + r) * C + c0 + q));
+    *reinterpret_cast<uint4*>(&tile[r][q]) = v;
   }
   __syncthreads();
-  for (int cc = ty; cc < 64; cc += 4) {
-    const int gc = c0 + cc, gr = r0 + tx;
-    if (gc < C && gr < R) o[static_cast<size_t>(gc) * R + gr] = tile[tx][cc];
+  const int lane = threadIdx.x & 31, wv = threadIdx.x >> 5;  // 8 warps
+  for (int i = wv; i < 2 * 8; i += 8) {
+    const int col = (i & 1) * 32 + lane;   // tile column = destination row
+    const int rq = (i >> 1) * 8;           // 8 tile rows = 8 destination columns
+    if (c0 + col < C && r0 + rq < R)
+      tile_store_out(tile, o + static_cast<size_t>(c0 + col) * R + r0 + rq, col, rq, R - (r0 + rq));
   }
 }
 
 // Token-major [Tk, C] (rows grouped by expert) -> [C, Kp]: token p of expert
 // e goes to column kseg[e] + p - offsets[e]; every other column is zero.
+// C % 8 == 0, Kp % 64 == 0.
 __global__ void __launch_bounds__(256) transpose_segments_kernel(const __nv_bfloat16* __restrict__ src,
                                                                  const int32_t* __restrict__ offsets,
                                                                  __nv_bfloat16* __restrict__ dst, int Tk, int C,
                                                                  int Kp, int E) {
-  __shared__ __nv_bfloat16 tile[64][66];
+  __shared__ __align__(16) __nv_bfloat16 tile[64][kTp];
   __shared__ int off_s[kMaxE + 1];
   __shared__ int kseg_s[kMaxE + 1];
+  __shared__ int srow[64];
   pdl_enter();
   if (threadIdx.x == 0) {
     int prev = 0, ks = 0;
@@ -201,14 +232,11 @@ __global__ void __launch_bounds__(256) transpose_segments_kernel(const __nv_bflo
       kseg_s[e] = ks;
       prev = o;
     }
-    kseg_s[0] = 0;
   }
   __syncthreads();
   const int k0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
-  // Rows of the tile: destination columns k0 + r.
-  for (int r = ty; r < 64; r += 4) {
-    const int kk = k0 + r;
+  if (threadIdx.x < 64) {
+    const int kk = k0 + threadIdx.x;
     int p = -1;
     if (kk < kseg_s[E]) {
       int e = 0;
@@ -216,13 +244,23 @@ __global__ void __launch_bounds__(256) transpose_segments_kernel(const __nv_bflo
       const int local = kk - kseg_s[e];
       if (local < off_s[e + 1] - off_s[e]) p = off_s[e] + local;
     }
-    const int gc = c0 + tx;
-    tile[r][tx] = (p >= 0 && gc < C) ? src[static_cast<size_t>(p) * C + gc] : __float2bfloat16(0.0f);
+    srow[threadIdx.x] = p;
   }
   __syncthreads();
-  for (int cc = ty; cc < 64; cc += 4) {
-    const int gc = c0 + cc, kk = k0 + tx;
-    if (gc < C && kk < Kp) dst[static_cast<size_t>(gc) * Kp + kk] = tile[tx][cc];
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int r = i >> 3, q = (i & 7) * 8;
+    const int p = srow[r];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (p >= 0 && c0 + q < C) v = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(p) * C + c0 + q));
+    *reinterpret_cast<uint4*>(&tile[r][q]) = v;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wv = threadIdx.x >> 5;
+  for (int i = wv; i < 2 * 8; i += 8) {
+    const int col = (i & 1) * 32 + lane;   // channel = destination row
+    const int rq = (i >> 1) * 8;           // 8 padded-token columns
+    if (c0 + col < C && k0 + rq < Kp)
+      tile_store_out(tile, dst + static_cast<size_t>(c0 + col) * Kp + k0 + rq, col, rq, Kp - (k0 + rq));
   }
 }
 
