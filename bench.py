@@ -168,10 +168,11 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- the layer
 class Layer:
-    """Device-resident inputs and buffers of one workload.  step() runs the
-    whole hot path through the C ABI; with `ev` (5 CUDA events) it records
-    them before the router, after dispatch, after gate/up, after down and
-    after combine."""
+    """Device-resident inputs, scratch and output of one workload.  step()
+    runs the whole hot path as one moe_forward_ex call through the C ABI;
+    with `ev` (5 CUDA events) the library records them before the router,
+    after dispatch, after gate/up, after down and after combine.  The
+    routing and intermediates are views into the scratch."""
 
     def __init__(self, wl, tensors, device):
         from sparse_mixture_experts_50_b300 import binding as B
@@ -182,6 +183,7 @@ class Layer:
         g = {n: v.to(dev, non_blocking=False) for n, v in tensors.items()}
         self.x, self.Wg, self.W1, self.W3, self.W2 = g["x"], g["Wg"], g["W1"], g["W3"], g["W2"]
         self.gamma = g.get("gamma")
+        self.w8 = None
         if wl.w8:
             # Weight preparation (once, outside any timed region): per-row
             # int8 codes and fp32 scales on the GPU; the bf16 copies go.
@@ -189,46 +191,20 @@ class Layer:
             self.W3q, self.W3s = B.moe_quantize_int8(self.W3)
             self.W2q, self.W2s = B.moe_quantize_int8(self.W2)
             self.W1 = self.W3 = self.W2 = None
-        dt = wl.torch_dtype
-        self.xn = torch.empty((T, d), dtype=dt, device=dev) if wl.block else None
-        self.idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-        self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
-        self.counts = torch.empty(E, dtype=torch.int32, device=dev)
-        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
-        self.row_src = torch.empty(T * k, dtype=torch.int32, device=dev)
-        self.slot_pos = torch.empty(T * k, dtype=torch.int32, device=dev)
-        self.x_perm = torch.empty((T * k, d), dtype=dt, device=dev)
-        self.h = torch.empty((T * k, F), dtype=dt, device=dev)
-        self.y = torch.empty((T * k, d), dtype=dt, device=dev)
-        self.out = torch.empty((T, d), dtype=dt, device=dev)
+            self.w8 = (self.W1q, self.W1s, self.W3q, self.W3s, self.W2q, self.W2s)
+        dtype = B.MOE_DTYPE_BF16 if wl.dtype == "bf16" else B.MOE_DTYPE_F32
+        self.ws = B.workspace(T, d, F, E, k, dtype, device=dev)
+        v = B.workspace_views(self.ws, T, d, F, E, k, dtype)
+        self.idx, self.w, self.counts, self.offsets = v["idx"], v["w"], v["counts"], v["offsets"]
+        self.row_src, self.slot_pos, self.x_perm, self.h, self.y = (v["row_src"], v["slot_pos"], v["x_perm"], v["h"],
+                                                                    v["y"])
+        self.xn = v["xn"] if wl.block else None
+        self.out = torch.empty((T, d), dtype=wl.torch_dtype, device=dev)
 
     def step(self, ev=None):
-        B, wl = self.B, self.wl
-        if ev is not None:
-            ev[0].record()
-        xin = self.x
-        if self.gamma is not None:
-            B.moe_rmsnorm(self.x, self.gamma, wl.eps, xn=self.xn)
-            xin = self.xn
-        B.moe_router_topk(xin, self.Wg, wl.k, self.idx, self.w)
-        B.moe_permute(xin, self.idx, wl.E, out=(self.counts, self.offsets, self.row_src, self.slot_pos, self.x_perm))
-        if ev is not None:
-            ev[1].record()
-        if wl.w8:
-            B.moe_expert_gate_up_w8(self.x_perm, self.offsets, self.W1q, self.W1s, self.W3q, self.W3s, self.h)
-        else:
-            B.moe_expert_gate_up(self.x_perm, self.offsets, self.W1, self.W3, self.h)
-        if ev is not None:
-            ev[2].record()
-        if wl.w8:
-            B.moe_expert_down_w8(self.h, self.offsets, self.W2q, self.W2s, self.y)
-        else:
-            B.moe_expert_down(self.h, self.offsets, self.W2, self.y)
-        if ev is not None:
-            ev[3].record()
-        B.moe_combine(self.y, self.slot_pos, self.w, wl.T, residual=self.x if wl.block else None, out=self.out)
-        if ev is not None:
-            ev[4].record()
+        wl = self.wl
+        self.B.moe_forward_ex(self.x, self.Wg, wl.k, self.ws, W1=self.W1, W3=self.W3, W2=self.W2, gamma=self.gamma,
+                              eps=wl.eps, w8=self.w8, out=self.out, events=ev)
         return self.out
 
 

@@ -143,6 +143,16 @@ int moe_combine(const void* y_perm, const int32_t* slot_pos, const float* topk_w
 size_t moe_forward_workspace_bytes(int T, int d, int dff, int E, int k, int dtype);
 
 /*
+ * Byte offsets of the layer's intermediates inside that scratch (host
+ * call, no device work): offs[0..9] = topk_idx [T,k] int32, topk_w [T,k]
+ * fp32, counts [E] int32, offsets [E+1] int32, row_src [T*k] int32,
+ * slot_pos [T*k] int32, x_perm [T*k,d], h_perm [T*k,dff], y_perm [T*k,d],
+ * xn [T,d] (block form); offs[10] = total bytes.  After a forward call these
+ * hold that call's values (the backward reads them as `saved`).
+ */
+int moe_forward_workspace_offsets(int T, int d, int dff, int E, int k, int dtype, size_t* offs);
+
+/*
  * The whole layer, a1..a6, on caller-provided scratch `workspace` of at least
  * moe_forward_workspace_bytes() bytes (256-byte aligned).  dtype selects the
  * bf16 tensor-core path or the fp32 path.
@@ -175,6 +185,24 @@ int moe_block_forward_ws(const void* x, const void* gamma, float eps, const void
 int moe_block_forward(const void* x, const void* gamma, float eps, const void* Wg,
                       const void* W1, const void* W3, const void* W2, void* out,
                       int T, int d, int dff, int E, int k, moe_stream_t stream);
+
+/*
+ * The layer with every option, on caller scratch, recording caller-created
+ * CUDA events at its step boundaries (for timing the steps of one call):
+ *  - gamma_opt != NULL selects the block form (as moe_block_forward_ws);
+ *  - W1q != NULL selects int8 expert weights (W1q..W2s as moe_forward_w8_ws;
+ *    W1, W3, W2 are then ignored; bf16 only);
+ *  - events (NULL, or 5 cudaEvent_t; NULL entries skipped) are recorded on
+ *    `stream` before the router, after dispatch, after the gate/up GEMM,
+ *    after the down GEMM and after the combine.
+ * workspace as moe_forward_ws.  Same results as the corresponding entry
+ * point.
+ */
+int moe_forward_ex(const void* x, const void* gamma_opt, float eps, const void* Wg, const void* W1,
+                   const void* W3, const void* W2, const int8_t* W1q, const float* W1s, const int8_t* W3q,
+                   const float* W3s, const int8_t* W2q, const float* W2s, void* out, int T, int d, int dff,
+                   int E, int k, int dtype, void* workspace, size_t workspace_bytes, void* const* events,
+                   moe_stream_t stream);
 
 /*
  * End-to-end call with HOST activations: copies x_host[T,d] (pinned host

@@ -40,11 +40,14 @@ SIGNATURES = {
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "moe_forward_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_forward_workspace_offsets": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "moe_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_forward_f32": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_block_forward_ws": (_I, [_P, _P, _F, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_block_forward": (_I, [_P, _P, _F, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "moe_forward_ex": (_I, [_P, _P, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
+                            _P, _P]),
     "moe_forward_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_quantize_int8": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -219,6 +222,26 @@ def moe_forward_workspace_bytes(T, d, dff, E, k, dtype=MOE_DTYPE_BF16) -> int:
     return int(lib().moe_forward_workspace_bytes(T, d, dff, E, k, dtype))
 
 
+def workspace_views(ws, T, d, dff, E, k, dtype=MOE_DTYPE_BF16):
+    """Views of the layer's intermediates inside a forward scratch tensor:
+    dict(idx, w, counts, offsets, row_src, slot_pos, x_perm, h, y, xn)."""
+    o = (_SZ * 11)()
+    _check("moe_forward_workspace_offsets", lib().moe_forward_workspace_offsets(T, d, dff, E, k, dtype, o))
+    fdt = torch.bfloat16 if dtype == MOE_DTYPE_BF16 else torch.float32
+    es = 2 if dtype == MOE_DTYPE_BF16 else 4
+
+    def view(i, n, dt, shape):
+        nbytes = n * (4 if dt in (torch.int32, torch.float32) else es)
+        return ws[o[i]:o[i] + nbytes].view(dt).reshape(shape)
+
+    Tk = T * k
+    return {"idx": view(0, Tk, torch.int32, (T, k)), "w": view(1, Tk, torch.float32, (T, k)),
+            "counts": view(2, E, torch.int32, (E,)), "offsets": view(3, E + 1, torch.int32, (E + 1,)),
+            "row_src": view(4, Tk, torch.int32, (Tk,)), "slot_pos": view(5, Tk, torch.int32, (Tk,)),
+            "x_perm": view(6, Tk * d, fdt, (Tk, d)), "h": view(7, Tk * dff, fdt, (Tk, dff)),
+            "y": view(8, Tk * d, fdt, (Tk, d)), "xn": view(9, T * d, fdt, (T, d))}
+
+
 def workspace(T, d, dff, E, k, dtype=MOE_DTYPE_BF16, device="cuda", host=False):
     """A uint8 device tensor big enough for moe_forward_ws (or moe_forward_host)."""
     fn = lib().moe_forward_host_workspace_bytes if host else lib().moe_forward_workspace_bytes
@@ -287,6 +310,31 @@ def moe_block_forward(x, gamma, eps, Wg, W1, W3, W2, k, out=None, stream=None):
         out = torch.empty_like(x)
     _check("moe_block_forward", lib().moe_block_forward(_p(x), _p(gamma), eps, _p(Wg), _p(W1), _p(W3), _p(W2),
                                                         _p(out), T, d, dff, E, k, _stream(stream)))
+    return out
+
+
+def moe_forward_ex(x, Wg, k, ws, W1=None, W3=None, W2=None, gamma=None, eps=0.0, w8=None, out=None, events=None,
+                   stream=None):
+    """The layer with every option on caller scratch `ws`: block form when
+    `gamma` is given, int8 experts when `w8` = (W1q, W1s, W3q, W3s, W2q, W2s);
+    `events` (5 torch.cuda.Event, already recorded once) are recorded at the
+    step boundaries.  Returns out[T,d]."""
+    _dev(x, Wg, W1, W3, W2, gamma, ws, out, *(w8 or ()))
+    T, d = x.shape
+    E = Wg.shape[0]
+    dff = (w8[0] if w8 is not None else W1).shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    ev = None
+    if events is not None:
+        for e in events:
+            if not e.cuda_event:  # torch creates an event on its first record
+                e.record()
+        ev = (ctypes.c_void_p * 5)(*[e.cuda_event for e in events])
+    q = [_p(v) for v in w8] if w8 is not None else [None] * 6
+    _check("moe_forward_ex", lib().moe_forward_ex(_p(x), _p(gamma), eps, _p(Wg), _p(W1), _p(W3), _p(W2), *q, _p(out),
+                                                  T, d, dff, E, k, _dtype(x), _p(ws), ws.numel(), ev,
+                                                  _stream(stream)))
     return out
 
 

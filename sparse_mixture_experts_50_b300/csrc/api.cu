@@ -63,6 +63,7 @@ int make_ctx(const void* dev_ptr, Ctx* ctx) {
   ctx->num_sms = d.num_sms;
   ctx->status = d.status;
   ctx->wait_ns = g_wait_ns.load();
+  ctx->max_rows_per_expert = 0;
   return MOE_OK;
 }
 
@@ -157,9 +158,17 @@ WsLayout ws_layout(int T, int d, int dff, int E, int k, int dtype) {
 
 // The layer on caller scratch; gamma != NULL selects the block form, w8 !=
 // NULL the int8 expert weights (W1, W3, W2 are then unused).
+// `events` (optional, 5 caller-created cudaEvent_t) are recorded before the
+// router, after dispatch, after gate/up, after down and after combine.
 int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, const void* W1, const void* W3,
                  const void* W2, void* out, int T, int d, int dff, int E, int k, int dtype, void* ws, size_t ws_bytes,
-                 const Ctx& c, cudaStream_t s, const W8Weights* w8 = nullptr) {
+                 const Ctx& cin, cudaStream_t s, const W8Weights* w8 = nullptr, void* const* events = nullptr) {
+  Ctx c = cin;
+  c.max_rows_per_expert = T;  // each token picks an expert at most once
+  auto mark = [&](int i) -> int {
+    if (events == nullptr || events[i] == nullptr) return MOE_OK;
+    return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess ? MOE_OK : MOE_ECUDA;
+  };
   const WsLayout L = ws_layout(T, d, dff, E, k, dtype);
   if (ws_bytes < L.total) return MOE_ENOMEM;
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -174,6 +183,7 @@ int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, co
   void* y = base + L.y;
   const int Tk = T * k;
   const void* xin = x;
+  MOE_TRY(mark(0));
   if (gamma != nullptr) {
     void* xn = base + L.xn;
     MOE_TRY(launch_rc(launch_rmsnorm(x, gamma, eps, xn, T, d, dtype, c, s)));
@@ -182,14 +192,19 @@ int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, co
   MOE_TRY(launch_rc(launch_router(xin, Wg, T, d, E, k, idx, w, nullptr, dtype, c, s)));
   MOE_TRY(launch_rc(launch_dispatch(idx, Tk, E, k, counts, offs, row_src, slot_pos, c, s)));
   MOE_TRY(launch_rc(launch_gather_rows(xin, row_src, x_perm, T, Tk, static_cast<size_t>(d) * esize(dtype), c, s)));
+  MOE_TRY(mark(1));
   if (w8 != nullptr) {
     MOE_TRY(launch_w8_gate_up(x_perm, offs, w8->q1, w8->s1, w8->q3, w8->s3, h, Tk, d, dff, E, c, s));
+    MOE_TRY(mark(2));
     MOE_TRY(launch_w8_down(h, offs, w8->q2, w8->s2, y, Tk, d, dff, E, c, s));
   } else {
     MOE_TRY(ffn_gate_up(x_perm, offs, W1, W3, h, Tk, d, dff, E, dtype, c, s));
+    MOE_TRY(mark(2));
     MOE_TRY(ffn_down(h, offs, W2, y, Tk, d, dff, E, dtype, c, s));
   }
+  MOE_TRY(mark(3));
   MOE_TRY(launch_rc(launch_combine(y, slot_pos, w, gamma != nullptr ? x : nullptr, out, T, d, k, dtype, c, s)));
+  MOE_TRY(mark(4));
   return MOE_OK;
 }
 
@@ -472,6 +487,16 @@ int moe_combine(const void* y_perm, const int32_t* slot_pos, const float* topk_w
   return launch_rc(launch_combine(y_perm, slot_pos, topk_w, residual_opt, out, T, d, k, dtype, c, stream));
 }
 
+int moe_forward_workspace_offsets(int T, int d, int dff, int E, int k, int dtype, size_t* offs) {
+  MOE_TRY(check_tokens(T, d, E, k, dtype));
+  if (dff <= 0) return MOE_EINVAL;
+  if (offs == nullptr) return MOE_EINVAL;
+  const WsLayout L = ws_layout(T, d, dff, E, k, dtype);
+  const size_t v[11] = {L.idx, L.w, L.counts, L.offs, L.row_src, L.slot_pos, L.x_perm, L.h, L.y, L.xn, L.total};
+  for (int i = 0; i < 11; ++i) offs[i] = v[i];
+  return MOE_OK;
+}
+
 size_t moe_forward_workspace_bytes(int T, int d, int dff, int E, int k, int dtype) {
   if (check_tokens(T, d, E, k, dtype) != MOE_OK || dff <= 0) return 0;
   return ws_layout(T, d, dff, E, k, dtype).total;
@@ -546,6 +571,27 @@ int moe_forward_host(const void* x_host, const void* Wg, const void* W1, const v
                        stream));
   if (cudaMemcpyAsync(out_host, out_dev, act_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MOE_ECUDA;
   return cudaStreamSynchronize(stream) == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
+
+int moe_forward_ex(const void* x, const void* gamma_opt, float eps, const void* Wg, const void* W1, const void* W3,
+                   const void* W2, const int8_t* W1q, const float* W1s, const int8_t* W3q, const float* W3s,
+                   const int8_t* W2q, const float* W2s, void* out, int T, int d, int dff, int E, int k, int dtype,
+                   void* workspace, size_t workspace_bytes, void* const* events, moe_stream_t stream) {
+  const bool w8 = W1q != nullptr;
+  if (w8 && dtype != MOE_DTYPE_BF16) return MOE_EUNSUPPORTED;
+  const W8Weights q{W1q, W1s, W3q, W3s, W2q, W2s};
+  // The shape and pointer checks of the plain layer; with int8 weights the
+  // bf16 ones are not used (Wg stands in for them in the null check).
+  MOE_TRY(check_forward(x, Wg, w8 ? Wg : W1, w8 ? Wg : W3, w8 ? Wg : W2, out, T, d, dff, E, k, dtype));
+  if (gamma_opt != nullptr) MOE_TRY(check_eps(eps));
+  if (T == 0) return MOE_OK;
+  if (w8) MOE_TRY(check_w8(q));
+  if (gamma_opt != nullptr && !aligned(gamma_opt, 16)) return MOE_EINVAL;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(out, &c));
+  return forward_impl(x, gamma_opt, eps, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype, workspace, workspace_bytes, c,
+                      stream, w8 ? &q : nullptr, events);
 }
 
 int moe_quantize_int8(const void* W, int rows, int cols, int8_t* q, float* scale, moe_stream_t stream) {

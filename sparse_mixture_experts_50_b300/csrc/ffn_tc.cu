@@ -825,9 +825,17 @@ int launch_mode(const void* A, const void* B0, const void* B1, GemmArgs a, const
   rc = smem_attr_once<SWIGLU, W8, SWAP>(c.device);
   if (rc != MOE_OK) return rc;
   // Upper bound on tiles: whole row blocks plus at most one partial block
-  // per expert that has rows (at most min(E, Tk) of them).
-  const long long max_tiles =
-      (static_cast<long long>(a.Tk) / P::rows + (a.E < a.Tk ? a.E : a.Tk)) * static_cast<long long>(a.n_tiles);
+  // per expert that has rows (at most min(E, Tk) of them); with a known
+  // bound on any expert's rows (the layer passes T: a token picks an expert
+  // at most once), also E times that bound's blocks.  The grid is sized
+  // from it, so a tight bound avoids a nearly empty last wave.
+  long long blocks = static_cast<long long>(a.Tk) / P::rows + (a.E < a.Tk ? a.E : a.Tk);
+  if (c.max_rows_per_expert > 0) {
+    const long long per = (static_cast<long long>(c.max_rows_per_expert < a.Tk ? c.max_rows_per_expert : a.Tk) +
+                           P::rows - 1) / P::rows;
+    if (per * a.E < blocks) blocks = per * a.E;
+  }
+  const long long max_tiles = blocks * static_cast<long long>(a.n_tiles);
   const int grid = balanced_grid(max_tiles, c.num_sms);
   launch_pdl(grouped_gemm_tc_kernel<SWIGLU, W8, SWAP>, grid, P::threads, P::smem_bytes, s, ta, tb0, tb1, a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;

@@ -18,6 +18,7 @@ struct Ctx {
   int num_sms;
   int* status;                 // device address of the per-device status word
   unsigned long long wait_ns;  // bounded-wait limit for spinning kernels
+  int max_rows_per_expert;     // expert GEMMs: known bound on any expert's rows (0: only Tk)
 };
 
 // Sets the calling thread's current device to the one owning `dev_ptr`

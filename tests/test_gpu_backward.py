@@ -62,9 +62,8 @@ def run_gpu(B, t, k, dout, entry="alloc"):
     else:
         grads = B.moe_backward(dd, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved)
     status_ok(B)
-    idx = saved[: T * k * 4].view(torch.int32).reshape(T, k).cpu().numpy()
-    w = saved[256 * ((T * k * 4 + 255) // 256):][: T * k * 4].view(torch.float32).reshape(T, k).cpu().numpy()
-    return grads, idx, w
+    v = B.workspace_views(saved, T, d, F, E, k)
+    return grads, v["idx"].cpu().numpy(), v["w"].cpu().numpy()
 
 
 def oracle_grads(t, k, dout, gidx, gw, experts=None):
