@@ -279,7 +279,7 @@ int forward_w8(const void* x, const void* Wg, const W8Weights& w8, void* out, in
 
 // ---- backward ---------------------------------------------------------------
 struct BwdLayout {
-  size_t dy, dop, wp, dl, dA, dB, dxp, W2t, W1t, W3t, Xt, dYt, Ht, dAt, dBt, part, total;
+  size_t dy, dop, wp, dl, dh, dA, dB, dxp, W2t, W1t, W3t, Xt, dYt, Ht, dAt, dBt, part, total;
   size_t kp;
 };
 
@@ -294,6 +294,7 @@ BwdLayout bwd_layout(int T, int d, int dff, int E, int k) {
   L.dop = o;   o = al256(o + Tk * d * 2);
   L.wp = o;    o = al256(o + Tk * 4);
   L.dl = o;    o = al256(o + Tk * 4);
+  L.dh = o;    o = al256(o + Tk * dff * 4);
   L.dA = o;    o = al256(o + Tk * dff * 2);
   L.dB = o;    o = al256(o + Tk * dff * 2);
   L.dxp = o;   o = al256(o + Tk * d * 2);
@@ -341,8 +342,10 @@ int backward_impl(const void* dout, const void* x, const void* Wg, const void* W
   MOE_TRY(launch_rc(launch_transpose_batched(W2, b + L.W2t, E, d, dff, s)));
   MOE_TRY(launch_rc(launch_transpose_batched(W1, b + L.W1t, E, dff, d, s)));
   MOE_TRY(launch_rc(launch_transpose_batched(W3, b + L.W3t, E, dff, d, s)));
-  // B3: dh = w (dout W2), a and b recomputed, SwiGLU derivative -> dA, dB.
-  MOE_TRY(launch_bwd_dswiglu(dop, wp, x_perm, offs, b + L.W2t, W1, W3, dA, dB, Tk, d, dff, E, c, s));
+  // B3: dh = w (dout W2) in fp32; a and b recomputed, SwiGLU derivative -> dA, dB.
+  float* dh = reinterpret_cast<float*>(b + L.dh);
+  MOE_TRY(launch_bwd_dh(dop, wp, offs, b + L.W2t, dh, Tk, d, dff, E, c, s));
+  MOE_TRY(launch_bwd_dsw(x_perm, dh, offs, W1, W3, dA, dB, Tk, d, dff, E, c, s));
   // B4: dx_perm = dA W1 + dB W3.
   MOE_TRY(launch_bwd_dx(dA, dB, offs, b + L.W1t, b + L.W3t, dxp, Tk, d, dff, E, c, s));
   // B5: un-permute + router path -> dx.

@@ -3,27 +3,28 @@
 // Transformer - 05 Mixtral", section 04, SwiGLU: y = W2 (silu(W1 x) * W3 x)).
 // For the rows p of expert e, with dout gathered per routed row and w_p the
 // row's gate weight:
-//   dh = w_p (dout W2_e),  a = x W1_e^T,  b = x W3_e^T,
-//   da = dh * b * silu'(a),  db = dh * silu(a)                    (DSWIGLU)
+//   dh = w_p (dout W2_e)                                           (DH, fp32)
+//   a = x W1_e^T,  b = x W3_e^T,
+//   da = dh * b * silu'(a),  db = dh * silu(a)                     (DSW)
 //   dx_perm = da W1_e + db W3_e                                    (DX)
 //   dW2_e = dy^T h,  dW1_e = da^T x,  dW3_e = db^T x               (WGRAD)
 //
 // One persistent tcgen05 kernel template, one CTA per SM, warp-specialised
 // like the forward kernel (warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5
 // epilogue), every operand K-major and staged by TMA with the 128-byte
-// swizzle.  The weight operands of DSWIGLU and DX are the transposed copies
+// swizzle.  The weight operands of DH and DX are the transposed copies
 // W2t [E,F,d], W1t and W3t [E,d,F]; WGRAD reads token-major activations
 // transposed to [channels, tokens] with each expert's tokens padded to a
 // multiple of 64 (zeros), so that every K step of an expert starts on a
 // 128-byte boundary.
-//   DSWIGLU  tile 128 rows x 128 h columns; two K=d passes: dout W2 (N=128)
-//            into columns 0-127, then a and b together (N=256, the W1 rows
-//            then the W3 rows of the tile's columns, as in the forward's
-//            gate/up GEMM) into columns 128-383; the epilogue scales the first by w_p in
-//            fp32 (dout is gathered exactly, so dh is not exposed to a bf16
-//            rounding of w dout, which its 4096-term sum can amplify where
-//            it cancels), forms da, db in fp32 and rounds them to bf16.  a
-//            and b are recomputed, not saved.
+//   DH       tile 128 rows x 256 h columns, one K=d pass; the epilogue
+//            scales by w_p and stores fp32 (dout is gathered exactly and dh
+//            stays fp32: a bf16 rounding of w dout or of dh would be
+//            amplified by the 4096-term sum where it cancels).
+//   DSW      tile 128 rows x 128 h columns: a and b recomputed in one K=d
+//            pass over the W1 and W3 rows (N=256, as the forward's gate/up
+//            GEMM); the epilogue reads dh, forms da, db in fp32 and rounds
+//            them to bf16.
 //   DX       tile 128 rows x 256 columns of dx_perm; two K=F passes (da with
 //            W1t, then db with W3t) into one accumulator; two accumulators
 //            alternate between tiles.
@@ -43,7 +44,7 @@
 namespace moe {
 namespace {
 
-enum { MODE_DSWIGLU = 0, MODE_DX = 1, MODE_WGRAD = 2 };
+enum { MODE_DH = 0, MODE_DX = 1, MODE_WGRAD = 2, MODE_DSW = 3 };
 
 constexpr int BM = 128;
 constexpr int BK = 64;
@@ -84,14 +85,15 @@ struct BwdArgs {
   int Tk;
   int K;                   // reduction length of one pass (d, F; WGRAD: unused)
   int b_rows;              // rows per expert in the B tensor(s)
-  int n_out;               // output columns (DSWIGLU: F, DX: d, WGRAD: N)
+  int n_out;               // output columns (DH, DSW: F; DX: d; WGRAD: N)
   int m_rows;              // WGRAD: output rows M
   int n_tiles;
-  // DSWIGLU: out0 = dA, out1 = dB [Tk, F]; DX: out0 = dx_perm [Tk, d]
+  // DSW: out0 = dA, out1 = dB [Tk, F]; DX: out0 = dx_perm [Tk, d]
   __nv_bfloat16* out0;
   __nv_bfloat16* out1;
-  float* outf;             // WGRAD: [E, M, N]
-  const float* w_perm;     // DSWIGLU: gate weight of each routed row [Tk]
+  float* outf;             // WGRAD: [E, M, N]; DH: dh [Tk, F]
+  const float* w_perm;     // DH: gate weight of each routed row [Tk]
+  const float* dh;         // DSW: dh [Tk, F] fp32
   int* status;
   unsigned long long wait_ns;
 };
@@ -129,6 +131,18 @@ __device__ __forceinline__ void warp_store_f32(uint32_t* stg, const uint32_t (&v
   __syncwarp();
 }
 
+// The transpose: rows r < rows of src (row stride ld, 32 fp32 each) into
+// the lanes (lane = row, v[i] = column i), reading one 128-byte row per
+// instruction.
+__device__ __forceinline__ void warp_load_f32(uint32_t* stg, const float* src, size_t ld, int rows, int lane,
+                                              float (&v)[32]) {
+  for (int r = 0; r < rows; ++r) stg[r * STG_PITCH + lane] = __float_as_uint(__ldg(src + r * ld + lane));
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(stg[lane * STG_PITCH + i]);
+  __syncwarp();
+}
+
 // The warp's 32 rows x 32 bf16 columns (lane = row, pk[i] = columns 2i,
 // 2i+1) to dst[r * ld + ...] for r < rows: two 64-byte rows per instruction.
 __device__ __forceinline__ void warp_store_bf16(uint32_t* stg, const uint32_t (&pk)[16], __nv_bfloat16* dst,
@@ -144,14 +158,12 @@ __device__ __forceinline__ void warp_store_bf16(uint32_t* stg, const uint32_t (&
 
 template <int MODE>
 struct Shape {
-  static constexpr int passes = MODE == MODE_DSWIGLU ? 2 : (MODE == MODE_DX ? 2 : 1);
-  static constexpr int n_tile = MODE == MODE_DSWIGLU ? BNH : 2 * BNH;   // output columns per tile
-  static constexpr int b_boxes = MODE == MODE_DSWIGLU ? 1 : 2;
-  static constexpr int acc_cols = MODE == MODE_DSWIGLU ? 3 * BNH : 2 * BNH;
-  static constexpr int n_acc = MODE == MODE_DSWIGLU ? 1 : 2;             // accumulators in flight
+  static constexpr int passes = MODE == MODE_DX ? 2 : 1;
+  static constexpr int n_tile = MODE == MODE_DSW ? BNH : 2 * BNH;   // output columns per tile
+  static constexpr int acc_cols = 2 * BNH;
+  static constexpr int n_acc = 2;                                    // accumulators in flight
   static constexpr int tmem_cols = 512;
-  static constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, b_boxes * BNH);
-  static constexpr uint32_t idesc_wide = ptx::idesc_bf16_f32(BM, 2 * BNH);  // DSWIGLU pass 1
+  static constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, 2 * BNH);
 };
 
 // Tensor maps per pass: A (token rows or, WGRAD, channel rows) and B.
@@ -272,19 +284,15 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
             brow = e * args.b_rows + n * S::n_tile;
           }
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          // DSWIGLU pass 1 stages two B boxes from two tensors (W1, W3) at
-          // the same rows; DX and WGRAD two consecutive 128-row boxes.
-          const bool wide = MODE == MODE_DSWIGLU ? pass == 1 : S::b_boxes == 2;
-          const int bytes = A_BYTES + (wide ? 2 : 1) * BNH * BK * 2;
-          ptx::mbar_arrive_expect_tx(&ctl->full[stage], bytes);
+          // DSW stages the W1 and the W3 rows of its 128 h columns; the
+          // other modes two consecutive 128-row boxes of one tensor.
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
           ptx::tma_load_2d(sa, &maps.a[pass], &ctl->full[stage], kx, arow);
           ptx::tma_load_2d(sa + A_BYTES, &maps.b[pass], &ctl->full[stage], kx, brow);
-          if (wide) {
-            if (MODE == MODE_DSWIGLU)
-              ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[2], &ctl->full[stage], kx, brow);
-            else
-              ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[pass], &ctl->full[stage], kx, brow + BNH);
-          }
+          if (MODE == MODE_DSW)
+            ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[1], &ctl->full[stage], kx, brow);
+          else
+            ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[pass], &ctl->full[stage], kx, brow + BNH);
           filled |= 1u << stage;
           last_parity[stage] = phase;
           if (++stage == STAGES) {
@@ -322,12 +330,11 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
             break;
           }
           ptx::tc_fence_after();
-          // DSWIGLU: pass 0 (N=128) into columns 0-127, pass 1 (N=256) into
-          // 128-383; otherwise every pass adds into the same accumulator.
+          // Every pass adds into the same accumulator (DX: da W1 + db W3).
           const int pass = MODE == MODE_WGRAD ? 0 : kb / kb_pass;
           const int kin = MODE == MODE_WGRAD ? kb : kb - pass * kb_pass;
-          const uint32_t d_tmem = d0 + (MODE == MODE_DSWIGLU ? static_cast<uint32_t>(pass * BNH) : 0u);
-          const uint32_t idesc = (MODE == MODE_DSWIGLU && pass == 1) ? S::idesc_wide : S::idesc;
+          const uint32_t d_tmem = d0;
+          const uint32_t idesc = S::idesc;
           const bool first = MODE == MODE_DX ? (kb == 0) : (kin == 0);
           const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
@@ -373,38 +380,52 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * S::acc_cols);
       uint32_t* stg = stage_blocks + quad * STG_WORDS;
-      if (MODE == MODE_DSWIGLU) {
+      if (MODE == MODE_DH) {
         const int row0 = ctl->seg[e] + m * BM + quad * 32;  // the warp's first row
         const int rows = max(0, min(32, ctl->seg[e + 1] - row0));
-        const bool row_ok = lane < rows;
-        const int col0 = n * BNH;
-        const float wp = row_ok ? __ldg(args.w_perm + row0 + lane) : 0.0f;
+        const int col0 = n * 2 * BNH;
+        const float wp = lane < rows ? __ldg(args.w_perm + row0 + lane) : 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < BNH; c += 32) {
-          uint32_t dh[32], av[32], bv[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c, dh);
-          ptx::tmem_ld_32x32b_x32(t_row + BNH + c, av);
-          ptx::tmem_ld_32x32b_x32(t_row + 2 * BNH + c, bv);
+        for (int c = 0; c < 2 * BNH; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c, v);
           ptx::tmem_ld_wait();
           if (rows > 0 && col0 + c < args.n_out) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(wp * __uint_as_float(v[i]));
+            warp_store_f32(stg, v, args.outf + static_cast<size_t>(row0) * args.n_out + col0 + c, args.n_out, rows,
+                           lane);
+          }
+        }
+      } else if (MODE == MODE_DSW) {
+        const int row0 = ctl->seg[e] + m * BM + quad * 32;
+        const int rows = max(0, min(32, ctl->seg[e + 1] - row0));
+        const int col0 = n * BNH;
+#pragma unroll 1
+        for (int c = 0; c < BNH; c += 32) {
+          uint32_t av[32], bv[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c, av);
+          ptx::tmem_ld_32x32b_x32(t_row + BNH + c, bv);
+          ptx::tmem_ld_wait();
+          if (rows > 0 && col0 + c < args.n_out) {
+            const size_t base = static_cast<size_t>(row0) * args.n_out + col0 + c;
+            float g[32];
+            warp_load_f32(stg, args.dh + base, args.n_out, rows, lane, g);
             uint32_t pa[16], pb[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               float da[2], db[2];
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const float g = wp * __uint_as_float(dh[2 * i + h]);
                 const float a = __uint_as_float(av[2 * i + h]);
                 const float b = __uint_as_float(bv[2 * i + h]);
                 const float s = 1.0f / (1.0f + __expf(-a));
-                const float silu = a * s;
-                da[h] = g * b * (s * (1.0f + a * (1.0f - s)));
-                db[h] = g * silu;
+                da[h] = g[2 * i + h] * b * (s * (1.0f + a * (1.0f - s)));
+                db[h] = g[2 * i + h] * (a * s);
               }
               pa[i] = pack_bf16x2(da[0], da[1]);
               pb[i] = pack_bf16x2(db[0], db[1]);
             }
-            const size_t base = static_cast<size_t>(row0) * args.n_out + col0 + c;
             warp_store_bf16(stg, pa, args.out0 + base, args.n_out, rows, lane);
             warp_store_bf16(stg, pb, args.out1 + base, args.n_out, rows, lane);
           }
@@ -534,18 +555,39 @@ size_t bwd_kpad_cols(int Tk, int E) {
   return (cols + KPAD - 1) / KPAD * KPAD;
 }
 
-int launch_bwd_dswiglu(const void* dout_perm, const float* w_perm, const void* x_perm, const int32_t* offsets,
-                       const void* W2t, const void* W1, const void* W3, void* dA, void* dB, int Tk, int d, int dff,
-                       int E, const Ctx& c, cudaStream_t s) {
+int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2t, float* dh,
+                  int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s) {
   if (Tk <= 0) return MOE_OK;
   Maps m;
   int rc = make_tmap(&m.a[0], dout_perm, d, Tk);
-  if (rc == MOE_OK) rc = make_tmap(&m.a[1], x_perm, d, Tk);
-  if (rc == MOE_OK) m.a[2] = m.a[1];  // unused
   if (rc == MOE_OK) rc = make_tmap(&m.b[0], W2t, d, static_cast<uint64_t>(E) * dff);
-  if (rc == MOE_OK) rc = make_tmap(&m.b[1], W1, d, static_cast<uint64_t>(E) * dff);
-  if (rc == MOE_OK) rc = make_tmap(&m.b[2], W3, d, static_cast<uint64_t>(E) * dff);
   if (rc != MOE_OK) return rc;
+  m.a[1] = m.a[2] = m.a[0];
+  m.b[1] = m.b[2] = m.b[0];
+  BwdArgs a = {};
+  a.offsets = offsets;
+  a.E = E;
+  a.Tk = Tk;
+  a.K = d;
+  a.b_rows = dff;
+  a.n_out = dff;
+  a.n_tiles = (dff + 2 * BNH - 1) / (2 * BNH);
+  a.outf = dh;
+  a.w_perm = w_perm;
+  const long long max_tiles = (static_cast<long long>(Tk) / BM + (E < Tk ? E : Tk)) * a.n_tiles;
+  return launch_bwd<MODE_DH>(m, a, max_tiles, c, s);
+}
+
+int launch_bwd_dsw(const void* x_perm, const float* dh, const int32_t* offsets, const void* W1, const void* W3,
+                   void* dA, void* dB, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s) {
+  if (Tk <= 0) return MOE_OK;
+  Maps m;
+  int rc = make_tmap(&m.a[0], x_perm, d, Tk);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[0], W1, d, static_cast<uint64_t>(E) * dff);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[1], W3, d, static_cast<uint64_t>(E) * dff);
+  if (rc != MOE_OK) return rc;
+  m.a[1] = m.a[2] = m.a[0];
+  m.b[2] = m.b[1];
   BwdArgs a = {};
   a.offsets = offsets;
   a.E = E;
@@ -556,9 +598,9 @@ int launch_bwd_dswiglu(const void* dout_perm, const float* w_perm, const void* x
   a.n_tiles = (dff + BNH - 1) / BNH;
   a.out0 = static_cast<__nv_bfloat16*>(dA);
   a.out1 = static_cast<__nv_bfloat16*>(dB);
-  a.w_perm = w_perm;
+  a.dh = dh;
   const long long max_tiles = (static_cast<long long>(Tk) / BM + (E < Tk ? E : Tk)) * a.n_tiles;
-  return launch_bwd<MODE_DSWIGLU>(m, a, max_tiles, c, s);
+  return launch_bwd<MODE_DSW>(m, a, max_tiles, c, s);
 }
 
 int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const void* W1t, const void* W3t,
