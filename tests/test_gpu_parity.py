@@ -385,3 +385,27 @@ def test_full_size_sampled(B, name):
         ref = ref + O.f64(cpu["x"][s])
     check_close(got, ref, "bf16", f"{name} out")
     print(f"{name}: near-tie tokens {n_tie}, routed differently {n_diff}, expert counts {counts.tolist()}")
+
+
+@pytest.mark.parametrize("T,E,k,d", [(1, 8, 2, 256), (7, 8, 2, 4096), (16, 8, 2, 4096), (33, 8, 2, 512),
+                                     (64, 8, 2, 1024), (16, 64, 8, 256), (100, 8, 1, 512)])
+def test_layer_routing_tables_match_step_entry_points(B, T, E, k, d):
+    """The layer call's routing, dispatch tables and permuted rows (read from
+    its scratch) equal those of moe_router_topk + moe_permute bit for bit."""
+    r = np.random.default_rng(T * 131 + E)
+    F = 128
+    x = torch.from_numpy(r.standard_normal((T, d))).to(torch.bfloat16)
+    Wg = torch.from_numpy(r.standard_normal((E, d)) * 0.02).to(torch.bfloat16)
+    W = [torch.from_numpy(r.standard_normal(s) * 0.05).to(torch.bfloat16) for s in ((E, F, d), (E, F, d), (E, d, F))]
+    g = [dev(v) for v in (x, Wg, *W)]
+    ws = B.workspace(T, d, F, E, k, B.MOE_DTYPE_BF16)
+    B.moe_forward_ws(*g, k, ws)
+    status_ok(B)
+    v = B.workspace_views(ws, T, d, F, E, k)
+    idx, w = B.moe_router_topk(g[0], g[1], k)
+    counts, offsets, row_src, slot_pos, x_perm = B.moe_permute(g[0], idx, E)
+    status_ok(B)
+    assert torch.equal(v["idx"], idx) and torch.equal(v["w"], w)
+    assert torch.equal(v["counts"], counts) and torch.equal(v["offsets"], offsets)
+    assert torch.equal(v["row_src"], row_src) and torch.equal(v["slot_pos"], slot_pos)
+    assert torch.equal(v["x_perm"], x_perm)
