@@ -279,14 +279,13 @@ int forward_w8(const void* x, const void* Wg, const W8Weights& w8, void* out, in
 
 // ---- backward ---------------------------------------------------------------
 struct BwdLayout {
-  size_t dy, dop, wp, dl, dh, dA, dB, dxp, W2t, W1t, W3t, Xt, dYt, Ht, dAt, dBt, part, total;
+  size_t dy, dop, wp, dl, dh, dA, dB, dxp, Xt, dYt, Ht, dAt, dBt, part, total;
   size_t kp;
 };
 
 BwdLayout bwd_layout(int T, int d, int dff, int E, int k) {
   const size_t Tk = static_cast<size_t>(T) * k;
   const size_t kp = bwd_kpad_cols(static_cast<int>(Tk), E);
-  const size_t wsz = static_cast<size_t>(E) * dff * d * 2;
   BwdLayout L;
   size_t o = 0;
   L.kp = kp;
@@ -298,9 +297,6 @@ BwdLayout bwd_layout(int T, int d, int dff, int E, int k) {
   L.dA = o;    o = al256(o + Tk * dff * 2);
   L.dB = o;    o = al256(o + Tk * dff * 2);
   L.dxp = o;   o = al256(o + Tk * d * 2);
-  L.W2t = o;   o = al256(o + wsz);
-  L.W1t = o;   o = al256(o + wsz);
-  L.W3t = o;   o = al256(o + wsz);
   L.Xt = o;    o = al256(o + kp * d * 2);
   L.dYt = o;   o = al256(o + kp * d * 2);
   L.Ht = o;    o = al256(o + kp * dff * 2);
@@ -338,16 +334,12 @@ int backward_impl(const void* dout, const void* x, const void* Wg, const void* W
   const int kp = static_cast<int>(L.kp);
   // B1-B2: expert-output and gate-weight gradients, softmax over the k chosen.
   MOE_TRY(launch_rc(launch_route_bwd(dout, y_perm, slot_pos, w, dy, dop, wp, dl, T, d, k, c, s)));
-  // K-major copies of the weights for the input-gradient GEMMs.
-  MOE_TRY(launch_rc(launch_transpose_batched(W2, b + L.W2t, E, d, dff, s)));
-  MOE_TRY(launch_rc(launch_transpose_batched(W1, b + L.W1t, E, dff, d, s)));
-  MOE_TRY(launch_rc(launch_transpose_batched(W3, b + L.W3t, E, dff, d, s)));
   // B3: dh = w (dout W2) in fp32; a and b recomputed, SwiGLU derivative -> dA, dB.
   float* dh = reinterpret_cast<float*>(b + L.dh);
-  MOE_TRY(launch_bwd_dh(dop, wp, offs, b + L.W2t, dh, Tk, d, dff, E, c, s));
+  MOE_TRY(launch_bwd_dh(dop, wp, offs, W2, dh, Tk, d, dff, E, c, s));
   MOE_TRY(launch_bwd_dsw(x_perm, dh, offs, W1, W3, dA, dB, Tk, d, dff, E, c, s));
   // B4: dx_perm = dA W1 + dB W3.
-  MOE_TRY(launch_bwd_dx(dA, dB, offs, b + L.W1t, b + L.W3t, dxp, Tk, d, dff, E, c, s));
+  MOE_TRY(launch_bwd_dx(dA, dB, offs, W1, W3, dxp, Tk, d, dff, E, c, s));
   // B5: un-permute + router path -> dx.
   MOE_TRY(launch_rc(launch_dx_gather(dxp, slot_pos, idx, dl, Wg, dx, T, d, E, k, c, s)));
   // B6: dWg.

@@ -12,8 +12,11 @@
 // One persistent tcgen05 kernel template, one CTA per SM, warp-specialised
 // like the forward kernel (warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5
 // epilogue), every operand K-major and staged by TMA with the 128-byte
-// swizzle.  The weight operands of DH and DX are the transposed copies
-// W2t [E,F,d], W1t and W3t [E,d,F]; WGRAD reads token-major activations
+// swizzle, except the weight operands of DH and DX: those are read in
+// place, MN-major (W2 [E,d,F] for dh, W1 and W3 [E,F,d] for dx_perm: their
+// contiguous dimension is the GEMM's N), as four TMA boxes of 64 N columns x
+// 64 K rows per stage, described to tcgen05 with the transpose-B bit.  WGRAD
+// reads token-major activations
 // transposed to [channels, tokens] with each expert's tokens padded to a
 // multiple of 64 (zeros), so that every K step of an expert starts on a
 // 128-byte boundary.
@@ -26,7 +29,7 @@
 //            GEMM); the epilogue reads dh, forms da, db in fp32 and rounds
 //            them to bf16.
 //   DX       tile 128 rows x 256 columns of dx_perm; two K=F passes (da with
-//            W1t, then db with W3t) into one accumulator; two accumulators
+//            W1, then db with W3) into one accumulator; two accumulators
 //            alternate between tiles.
 //   WGRAD    per expert an [M, N] fp32 matrix, tile 128 x 256, K = the
 //            expert's padded token segment; an expert with no tokens gets
@@ -81,6 +84,7 @@ constexpr size_t SMEM_BYTES =
 
 struct BwdArgs {
   const int32_t* offsets;  // [E+1] routed-row boundaries
+  int b_krows;             // DH, DX: K rows per expert in the MN-major weight (d, F)
   int E;
   int Tk;
   int K;                   // reduction length of one pass (d, F; WGRAD: unused)
@@ -163,7 +167,8 @@ struct Shape {
   static constexpr int acc_cols = 2 * BNH;
   static constexpr int n_acc = 2;                                    // accumulators in flight
   static constexpr int tmem_cols = 512;
-  static constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, 2 * BNH);
+  static constexpr bool b_mn = MODE == MODE_DH || MODE == MODE_DX;  // weights read MN-major
+  static constexpr uint32_t idesc = b_mn ? ptx::idesc_bf16_f32_bmn(BM, 2 * BNH) : ptx::idesc_bf16_f32(BM, 2 * BNH);
 };
 
 // Tensor maps per pass: A (token rows or, WGRAD, channel rows) and B.
@@ -284,15 +289,25 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
             brow = e * args.b_rows + n * S::n_tile;
           }
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          // DSW stages the W1 and the W3 rows of its 128 h columns; the
-          // other modes two consecutive 128-row boxes of one tensor.
           ptx::mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
           ptx::tma_load_2d(sa, &maps.a[pass], &ctl->full[stage], kx, arow);
-          ptx::tma_load_2d(sa + A_BYTES, &maps.b[pass], &ctl->full[stage], kx, brow);
-          if (MODE == MODE_DSW)
-            ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[1], &ctl->full[stage], kx, brow);
-          else
-            ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[pass], &ctl->full[stage], kx, brow + BNH);
+          if (S::b_mn) {
+            // Four 64-column x 64-row boxes: N columns n*256 + 64i, K rows
+            // kx .. kx+63 of expert e.
+            const int krow = e * args.b_krows + kx;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              ptx::tma_load_2d(sa + A_BYTES + i * (64 * BK * 2), &maps.b[pass], &ctl->full[stage],
+                               n * S::n_tile + 64 * i, krow);
+          } else {
+            // DSW stages the W1 and the W3 rows of its 128 h columns; WGRAD
+            // two consecutive 128-row boxes of one tensor.
+            ptx::tma_load_2d(sa + A_BYTES, &maps.b[pass], &ctl->full[stage], kx, brow);
+            if (MODE == MODE_DSW)
+              ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[1], &ctl->full[stage], kx, brow);
+            else
+              ptx::tma_load_2d(sa + A_BYTES + BNH * BK * 2, &maps.b[pass], &ctl->full[stage], kx, brow + BNH);
+          }
           filled |= 1u << stage;
           last_parity[stage] = phase;
           if (++stage == STAGES) {
@@ -340,8 +355,11 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            ptx::umma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2),
-                           ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2), idesc, (first && kk == 0) ? 0u : 1u);
+            // MN-major B: a K step of 16 is two 8-row groups, 2048 bytes on.
+            const uint64_t bdesc = S::b_mn ? ptx::sdesc_mnmajor_sw128(sb + kk * 2048, 64 * BK * 2)
+                                           : ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2);
+            ptx::umma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2), bdesc, idesc,
+                           (first && kk == 0) ? 0u : 1u);
           }
           ptx::umma_commit(&ctl->empty[stage]);
           if (++stage == STAGES) {
@@ -504,13 +522,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 [rows, inner] -> 64 x 128 boxes, 128-byte swizzle, zero fill.
-int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows) {
+// Row-major bf16 [rows, inner] -> 64 x box_rows boxes, 128-byte swizzle, zero fill.
+int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, int box_rows = BNH) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return MOE_ECUDA;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {BK, BNH};
+  const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -555,12 +573,12 @@ size_t bwd_kpad_cols(int Tk, int E) {
   return (cols + KPAD - 1) / KPAD * KPAD;
 }
 
-int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2t, float* dh,
+int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2, float* dh,
                   int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s) {
   if (Tk <= 0) return MOE_OK;
   Maps m;
   int rc = make_tmap(&m.a[0], dout_perm, d, Tk);
-  if (rc == MOE_OK) rc = make_tmap(&m.b[0], W2t, d, static_cast<uint64_t>(E) * dff);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[0], W2, dff, static_cast<uint64_t>(E) * d, 64);  // MN-major: [E*d, F]
   if (rc != MOE_OK) return rc;
   m.a[1] = m.a[2] = m.a[0];
   m.b[1] = m.b[2] = m.b[0];
@@ -570,6 +588,7 @@ int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* off
   a.Tk = Tk;
   a.K = d;
   a.b_rows = dff;
+  a.b_krows = d;
   a.n_out = dff;
   a.n_tiles = (dff + 2 * BNH - 1) / (2 * BNH);
   a.outf = dh;
@@ -603,14 +622,14 @@ int launch_bwd_dsw(const void* x_perm, const float* dh, const int32_t* offsets, 
   return launch_bwd<MODE_DSW>(m, a, max_tiles, c, s);
 }
 
-int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const void* W1t, const void* W3t,
+int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const void* W1, const void* W3,
                   void* dx_perm, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s) {
   if (Tk <= 0) return MOE_OK;
   Maps m;
   int rc = make_tmap(&m.a[0], dA, dff, Tk);
   if (rc == MOE_OK) rc = make_tmap(&m.a[1], dB, dff, Tk);
-  if (rc == MOE_OK) rc = make_tmap(&m.b[0], W1t, dff, static_cast<uint64_t>(E) * d);
-  if (rc == MOE_OK) rc = make_tmap(&m.b[1], W3t, dff, static_cast<uint64_t>(E) * d);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[0], W1, d, static_cast<uint64_t>(E) * dff, 64);  // MN-major: [E*F, d]
+  if (rc == MOE_OK) rc = make_tmap(&m.b[1], W3, d, static_cast<uint64_t>(E) * dff, 64);
   if (rc != MOE_OK) return rc;
   m.a[2] = m.a[1];
   m.b[2] = m.b[1];
@@ -620,6 +639,7 @@ int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const 
   a.Tk = Tk;
   a.K = dff;
   a.b_rows = d;
+  a.b_krows = dff;
   a.n_out = d;
   a.n_tiles = (d + 2 * BNH - 1) / (2 * BNH);
   a.out0 = static_cast<__nv_bfloat16*>(dx_perm);

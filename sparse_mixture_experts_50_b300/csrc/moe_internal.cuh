@@ -87,11 +87,11 @@ int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* 
 // Backward (bf16 activations, fp32 weight gradients).
 size_t bwd_kpad_cols(int Tk, int E);
 int dwg_chunks(int T);
-int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2t, float* dh,
+int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2, float* dh,
                   int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 int launch_bwd_dsw(const void* x_perm, const float* dh, const int32_t* offsets, const void* W1, const void* W3,
                    void* dA, void* dB, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
-int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const void* W1t, const void* W3t,
+int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const void* W1, const void* W3,
                   void* dx_perm, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 int launch_bwd_wgrad(const void* At, const void* Bt, const int32_t* offsets, float* dW, int M, int N, int Tk,
                      int E, const Ctx& c, cudaStream_t s);

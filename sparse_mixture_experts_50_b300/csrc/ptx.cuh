@@ -220,6 +220,22 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return desc;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile stored with the
+// 128-byte swizzle, as TMA writes boxes of 64 contiguous MN elements x K rows
+// with CU_TENSOR_MAP_SWIZZLE_128B: each K row is 128 bytes, 8 K rows form a
+// 1024-byte swizzle atom (stride byte offset = 1024, between 8-row K groups),
+// and successive 64-element MN atoms are `mn_stride` bytes apart (leading
+// byte offset).  Version 1, base offset 0, swizzle mode 2.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  desc |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+  desc |= static_cast<uint64_t>(1024u >> 4) << 32;
+  desc |= static_cast<uint64_t>(1u) << 46;
+  desc |= static_cast<uint64_t>(2u) << 61;
+  return desc;
+}
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.
@@ -227,6 +243,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+
+// The same with B MN-major (bit 16, "transpose B").
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) { return idesc_bf16_f32(M, N) | (1u << 16); }
 
 }  // namespace ptx
 }  // namespace moe
