@@ -279,16 +279,13 @@ int forward_w8(const void* x, const void* Wg, const W8Weights& w8, void* out, in
 
 // ---- backward ---------------------------------------------------------------
 struct BwdLayout {
-  size_t dy, dop, wp, dl, dh, dA, dB, dxp, Xt, dYt, Ht, dAt, dBt, part, total;
-  size_t kp;
+  size_t dy, dop, wp, dl, dh, dA, dB, dxp, part, total;
 };
 
 BwdLayout bwd_layout(int T, int d, int dff, int E, int k) {
   const size_t Tk = static_cast<size_t>(T) * k;
-  const size_t kp = bwd_kpad_cols(static_cast<int>(Tk), E);
   BwdLayout L;
   size_t o = 0;
-  L.kp = kp;
   L.dy = o;    o = al256(o + Tk * d * 2);
   L.dop = o;   o = al256(o + Tk * d * 2);
   L.wp = o;    o = al256(o + Tk * 4);
@@ -297,17 +294,12 @@ BwdLayout bwd_layout(int T, int d, int dff, int E, int k) {
   L.dA = o;    o = al256(o + Tk * dff * 2);
   L.dB = o;    o = al256(o + Tk * dff * 2);
   L.dxp = o;   o = al256(o + Tk * d * 2);
-  L.Xt = o;    o = al256(o + kp * d * 2);
-  L.dYt = o;   o = al256(o + kp * d * 2);
-  L.Ht = o;    o = al256(o + kp * dff * 2);
-  L.dAt = o;   o = al256(o + kp * dff * 2);
-  L.dBt = o;   o = al256(o + kp * dff * 2);
   L.part = o;  o = al256(o + static_cast<size_t>(dwg_chunks(T)) * E * d * 4);
   L.total = o;
   return L;
 }
 
-// The backward, B1..B8, on caller scratch; `saved` is the scratch of the
+// The backward, B1..B7, on caller scratch; `saved` is the scratch of the
 // forward call (moe_forward_ws) on the same x and weights.
 int backward_impl(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
                   const void* saved, void* dx, float* dWg, float* dW1, float* dW3, float* dW2, int T, int d, int dff,
@@ -331,7 +323,6 @@ int backward_impl(const void* dout, const void* x, const void* Wg, const void* W
   void* dB = b + L.dB;
   void* dxp = b + L.dxp;
   const int Tk = T * k;
-  const int kp = static_cast<int>(L.kp);
   // B1-B2: expert-output and gate-weight gradients, softmax over the k chosen.
   MOE_TRY(launch_rc(launch_route_bwd(dout, y_perm, slot_pos, w, dy, dop, wp, dl, T, d, k, c, s)));
   // B3: dh = w (dout W2) in fp32; a and b recomputed, SwiGLU derivative -> dA, dB.
@@ -344,16 +335,11 @@ int backward_impl(const void* dout, const void* x, const void* Wg, const void* W
   MOE_TRY(launch_rc(launch_dx_gather(dxp, slot_pos, idx, dl, Wg, dx, T, d, E, k, c, s)));
   // B6: dWg.
   MOE_TRY(launch_rc(launch_dwg(x, idx, dl, reinterpret_cast<float*>(b + L.part), dWg, T, d, E, k, c, s)));
-  // B7: token-major -> [channels, padded tokens] for the weight gradients.
-  MOE_TRY(launch_rc(launch_transpose_segments(x_perm, offs, b + L.Xt, Tk, d, kp, E, s)));
-  MOE_TRY(launch_rc(launch_transpose_segments(dy, offs, b + L.dYt, Tk, d, kp, E, s)));
-  MOE_TRY(launch_rc(launch_transpose_segments(h, offs, b + L.Ht, Tk, dff, kp, E, s)));
-  MOE_TRY(launch_rc(launch_transpose_segments(dA, offs, b + L.dAt, Tk, dff, kp, E, s)));
-  MOE_TRY(launch_rc(launch_transpose_segments(dB, offs, b + L.dBt, Tk, dff, kp, E, s)));
-  // B8: dW2 = dy^T h, dW1 = dA^T x, dW3 = dB^T x per expert.
-  MOE_TRY(launch_bwd_wgrad(b + L.dYt, b + L.Ht, offs, dW2, d, dff, Tk, E, c, s));
-  MOE_TRY(launch_bwd_wgrad(b + L.dAt, b + L.Xt, offs, dW1, dff, d, Tk, E, c, s));
-  MOE_TRY(launch_bwd_wgrad(b + L.dBt, b + L.Xt, offs, dW3, dff, d, Tk, E, c, s));
+  // B7: dW2 = dy^T h, dW1 = dA^T x, dW3 = dB^T x per expert, from the
+  // token-major rows.
+  MOE_TRY(launch_bwd_wgrad(dy, h, offs, dW2, d, dff, Tk, E, c, s));
+  MOE_TRY(launch_bwd_wgrad(dA, x_perm, offs, dW1, dff, d, Tk, E, c, s));
+  MOE_TRY(launch_bwd_wgrad(dB, x_perm, offs, dW3, dff, d, Tk, E, c, s));
   return MOE_OK;
 }
 

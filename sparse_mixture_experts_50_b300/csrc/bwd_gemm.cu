@@ -12,14 +12,15 @@
 // One persistent tcgen05 kernel template, one CTA per SM, warp-specialised
 // like the forward kernel (warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5
 // epilogue), every operand K-major and staged by TMA with the 128-byte
-// swizzle, except the weight operands of DH and DX: those are read in
-// place, MN-major (W2 [E,d,F] for dh, W1 and W3 [E,F,d] for dx_perm: their
-// contiguous dimension is the GEMM's N), as four TMA boxes of 64 N columns x
-// 64 K rows per stage, described to tcgen05 with the transpose-B bit.  WGRAD
-// reads token-major activations
-// transposed to [channels, tokens] with each expert's tokens padded to a
-// multiple of 64 (zeros), so that every K step of an expert starts on a
-// 128-byte boundary.
+// swizzle.  The token rows are K-major; everything else is read in place
+// MN-major, as TMA boxes of 64 M or N columns x 64 K rows described to
+// tcgen05 with the transpose bits: the weights of DH and DX (W2 [E,d,F] for
+// dh, W1 and W3 [E,F,d] for dx_perm, whose contiguous dimension is the
+// GEMM's N) and both operands of WGRAD (the token-major activations
+// [Tk, channels], K = the expert's tokens).  An expert's last K block of
+// WGRAD may run into the next expert's rows: the MMA warp clears those rows
+// (up to the next 16-row MMA step) in shared memory and skips the steps
+// past them.
 //   DH       tile 128 rows x 256 h columns, one K=d pass; the epilogue
 //            scales by w_p and stores fp32 (dout is gathered exactly and dh
 //            stays fp32: a bf16 rounding of w dout or of dh would be
@@ -60,7 +61,7 @@ constexpr int STAGES = 4;
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr int MAX_E = 64;
-constexpr int KPAD = 64;                  // WGRAD: token segments padded to this
+constexpr int MN_BOX_BYTES = 64 * BK * 2; // one MN-major box: 64 columns x 64 K rows
 
 struct Ctl {
   uint64_t full[STAGES];
@@ -72,8 +73,8 @@ struct Ctl {
   int abort_flag;
   int tile_prefix[MAX_E + 1];
   int mtiles[MAX_E];
-  int seg[MAX_E + 1];    // row segments (M-grouped) / padded token segments (WGRAD)
-  int rows[MAX_E];       // WGRAD: real tokens of each expert
+  int seg[MAX_E + 1];    // routed-row segments
+  int rows[MAX_E];       // WGRAD: tokens of each expert
 };
 
 constexpr int STG_PITCH = 33;             // staging block row pitch (32-bit words)
@@ -124,6 +125,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The helpers below unroll their 32 rows fully (rows past `rows` are
+// predicated off), so that a warp has all its loads or stores in flight at
+// once instead of one row's latency after another.
+
 // The warp's 32 rows x 32 fp32 columns (lane = row, v[i] = column i) to
 // dst[r * ld + i] for r < rows: one coalesced 128-byte row per instruction.
 __device__ __forceinline__ void warp_store_f32(uint32_t* stg, const uint32_t (&v)[32], float* dst, size_t ld,
@@ -131,16 +136,23 @@ __device__ __forceinline__ void warp_store_f32(uint32_t* stg, const uint32_t (&v
 #pragma unroll
   for (int i = 0; i < 32; ++i) stg[lane * STG_PITCH + i] = v[i];
   __syncwarp();
-  for (int r = 0; r < rows; ++r) dst[r * ld + lane] = __uint_as_float(stg[r * STG_PITCH + lane]);
+#pragma unroll
+  for (int r = 0; r < 32; ++r)
+    if (r < rows) dst[r * ld + lane] = __uint_as_float(stg[r * STG_PITCH + lane]);
   __syncwarp();
 }
 
-// The transpose: rows r < rows of src (row stride ld, 32 fp32 each) into
-// the lanes (lane = row, v[i] = column i), reading one 128-byte row per
-// instruction.
-__device__ __forceinline__ void warp_load_f32(uint32_t* stg, const float* src, size_t ld, int rows, int lane,
-                                              float (&v)[32]) {
-  for (int r = 0; r < rows; ++r) stg[r * STG_PITCH + lane] = __float_as_uint(__ldg(src + r * ld + lane));
+// Rows r < rows of src (row stride ld, 32 fp32 each; lane = column), one
+// 128-byte row per instruction; rows past `rows` read as zero.
+__device__ __forceinline__ void warp_load_rows_f32(const float* src, size_t ld, int rows, int lane, float (&t)[32]) {
+#pragma unroll
+  for (int r = 0; r < 32; ++r) t[r] = r < rows ? __ldg(src + r * ld + lane) : 0.0f;
+}
+
+// The transpose of what warp_load_rows_f32 read: lane = row, v[i] = column i.
+__device__ __forceinline__ void warp_transpose_f32(uint32_t* stg, const float (&t)[32], int lane, float (&v)[32]) {
+#pragma unroll
+  for (int r = 0; r < 32; ++r) stg[r * STG_PITCH + lane] = __float_as_uint(t[r]);
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(stg[lane * STG_PITCH + i]);
@@ -155,8 +167,11 @@ __device__ __forceinline__ void warp_store_bf16(uint32_t* stg, const uint32_t (&
   for (int i = 0; i < 16; ++i) stg[lane * 17 + i] = pk[i];
   __syncwarp();
   const int half = lane >> 4, w = lane & 15;
-  for (int r = half; r < rows; r += 2)
-    reinterpret_cast<uint32_t*>(dst + r * ld)[w] = stg[r * 17 + w];
+#pragma unroll
+  for (int r2 = 0; r2 < 32; r2 += 2) {
+    const int r = r2 + half;
+    if (r < rows) reinterpret_cast<uint32_t*>(dst + r * ld)[w] = stg[r * 17 + w];
+  }
   __syncwarp();
 }
 
@@ -167,8 +182,11 @@ struct Shape {
   static constexpr int acc_cols = 2 * BNH;
   static constexpr int n_acc = 2;                                    // accumulators in flight
   static constexpr int tmem_cols = 512;
-  static constexpr bool b_mn = MODE == MODE_DH || MODE == MODE_DX;  // weights read MN-major
-  static constexpr uint32_t idesc = b_mn ? ptx::idesc_bf16_f32_bmn(BM, 2 * BNH) : ptx::idesc_bf16_f32(BM, 2 * BNH);
+  static constexpr bool a_mn = MODE == MODE_WGRAD;                               // activations MN-major
+  static constexpr bool b_mn = MODE == MODE_DH || MODE == MODE_DX || MODE == MODE_WGRAD;
+  static constexpr uint32_t idesc = a_mn   ? ptx::idesc_bf16_f32_mn(BM, 2 * BNH)
+                                    : b_mn ? ptx::idesc_bf16_f32_bmn(BM, 2 * BNH)
+                                           : ptx::idesc_bf16_f32(BM, 2 * BNH);
 };
 
 // Tensor maps per pass: A (token rows or, WGRAD, channel rows) and B.
@@ -215,7 +233,6 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
   if (threadIdx.x == 0) {
     int prev = 0;
     int run = 0;
-    int kseg = 0;
     ctl->tile_prefix[0] = 0;
     for (int e = 0; e <= args.E; ++e) {
       int o = args.offsets[e];
@@ -225,15 +242,13 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
       }
       if (e > 0) {
         const int n_e = o - prev;
+        ctl->seg[e - 1] = prev;
         if (MODE == MODE_WGRAD) {
           ctl->rows[e - 1] = n_e;
-          ctl->seg[e - 1] = kseg;
-          kseg += (n_e + KPAD - 1) / KPAD * KPAD;
           const int mt = (args.m_rows + BM - 1) / BM;
           ctl->mtiles[e - 1] = mt;
           run += mt * args.n_tiles;
         } else {
-          ctl->seg[e - 1] = prev;
           const int mt = (n_e + BM - 1) / BM;
           ctl->mtiles[e - 1] = mt;
           run += mt * args.n_tiles;
@@ -242,7 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
       }
       prev = o;
     }
-    ctl->seg[args.E] = MODE == MODE_WGRAD ? kseg : prev;
+    ctl->seg[args.E] = prev;
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -253,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
 
   // K steps of a tile (all passes).
   auto tile_kblocks = [&](int e) -> int {
-    if (MODE == MODE_WGRAD) return (ctl->seg[e + 1] - ctl->seg[e]) / BK;
+    if (MODE == MODE_WGRAD) return (ctl->rows[e] + BK - 1) / BK;
     return S::passes * kb_pass;
   };
 
@@ -276,30 +291,34 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
             ok = false;
             break;
           }
-          int pass, kx, arow, brow;
-          if (MODE == MODE_WGRAD) {
-            pass = 0;
-            kx = ctl->seg[e] + kb * BK;
-            arow = m * BM;
-            brow = n * 2 * BNH;
-          } else {
-            pass = kb / kb_pass;
-            kx = (kb - pass * kb_pass) * BK;
-            arow = ctl->seg[e] + m * BM;
-            brow = e * args.b_rows + n * S::n_tile;
-          }
+          const int pass = MODE == MODE_WGRAD ? 0 : kb / kb_pass;
+          const int kx = (kb - pass * kb_pass) * BK;
+          const int arow = ctl->seg[e] + m * BM;
+          const int brow = e * args.b_rows + n * S::n_tile;
           uint8_t* sa = smem + stage * STAGE_BYTES;
           ptx::mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
-          ptx::tma_load_2d(sa, &maps.a[pass], &ctl->full[stage], kx, arow);
-          if (S::b_mn) {
+          if (MODE == MODE_WGRAD) {
+            // Two 64-channel boxes of A and four of B, K rows = the
+            // expert's tokens seg[e] + kb*64 .. +63.
+            const int krow = ctl->seg[e] + kb * BK;
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              ptx::tma_load_2d(sa + i * MN_BOX_BYTES, &maps.a[0], &ctl->full[stage], m * BM + 64 * i, krow);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              ptx::tma_load_2d(sa + A_BYTES + i * MN_BOX_BYTES, &maps.b[0], &ctl->full[stage],
+                               n * 2 * BNH + 64 * i, krow);
+          } else if (S::b_mn) {
+            ptx::tma_load_2d(sa, &maps.a[pass], &ctl->full[stage], kx, arow);
             // Four 64-column x 64-row boxes: N columns n*256 + 64i, K rows
             // kx .. kx+63 of expert e.
             const int krow = e * args.b_krows + kx;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              ptx::tma_load_2d(sa + A_BYTES + i * (64 * BK * 2), &maps.b[pass], &ctl->full[stage],
+              ptx::tma_load_2d(sa + A_BYTES + i * MN_BOX_BYTES, &maps.b[pass], &ctl->full[stage],
                                n * S::n_tile + 64 * i, krow);
           } else {
+            ptx::tma_load_2d(sa, &maps.a[pass], &ctl->full[stage], kx, arow);
             // DSW stages the W1 and the W3 rows of its 128 h columns; WGRAD
             // two consecutive 128-row boxes of one tensor.
             ptx::tma_load_2d(sa + A_BYTES, &maps.b[pass], &ctl->full[stage], kx, brow);
@@ -321,63 +340,96 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        int e, m, n;
-        decode_tile(ctl, args.E, tile, e, m, n);
-        const int nkb = tile_kblocks(e);
-        if (!ptx::mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, abort_flag, args.wait_ns)) {
-          raise_abort(ctl, args.status);
+    // -------------------------------------------------- MMA issuer
+    // Lane 0 waits and issues; the whole warp clears WGRAD's ragged rows.
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      int e, m, n;
+      decode_tile(ctl, args.E, tile, e, m, n);
+      const int nkb = tile_kblocks(e);
+      bool got = true;
+      if (lane == 0) {
+        got = ptx::mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, abort_flag, args.wait_ns);
+        if (!got) raise_abort(ctl, args.status);
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, got, 0)) break;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::acc_cols);
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (lane == 0) {
+          got = ptx::mbar_wait(&ctl->full[stage], phase, abort_flag, args.wait_ns);
+          if (!got) raise_abort(ctl, args.status);
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+          ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::acc_cols);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag, args.wait_ns)) {
-            raise_abort(ctl, args.status);
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          // Every pass adds into the same accumulator (DX: da W1 + db W3).
-          const int pass = MODE == MODE_WGRAD ? 0 : kb / kb_pass;
-          const int kin = MODE == MODE_WGRAD ? kb : kb - pass * kb_pass;
-          const uint32_t d_tmem = d0;
-          const uint32_t idesc = S::idesc;
-          const bool first = MODE == MODE_DX ? (kb == 0) : (kin == 0);
-          const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // MN-major B: a K step of 16 is two 8-row groups, 2048 bytes on.
-            const uint64_t bdesc = S::b_mn ? ptx::sdesc_mnmajor_sw128(sb + kk * 2048, 64 * BK * 2)
-                                           : ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2);
-            ptx::umma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2), bdesc, idesc,
-                           (first && kk == 0) ? 0u : 1u);
-          }
-          ptx::umma_commit(&ctl->empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+        // Every pass adds into the same accumulator (DX: da W1 + db W3).
+        const int pass = MODE == MODE_WGRAD ? 0 : kb / kb_pass;
+        const int kin = MODE == MODE_WGRAD ? kb : kb - pass * kb_pass;
+        const bool first = MODE == MODE_DX ? (kb == 0) : (kin == 0);
+        const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t sb = sa + A_BYTES;
+        int ksteps = BK / UMMA_K;
+        if (MODE == MODE_WGRAD) {
+          const int valid = ctl->rows[e] - kb * BK;  // >= 1
+          if (valid < BK) {
+            const int upto = (valid + UMMA_K - 1) / UMMA_K * UMMA_K;
+            ksteps = upto / UMMA_K;
+            // Rows valid .. upto-1 of the six boxes (A: 2, B: 4) hold the
+            // next expert's tokens: zero them.  A 128-byte row keeps its
+            // bytes under the swizzle, which only permutes its 16-byte chunks.
+            const int per_box = (upto - valid) * 8;
+            const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+            for (int i = lane; i < 6 * per_box; i += 32) {
+              const int box = i / per_box;
+              const int rem = i - box * per_box;
+              ptx::sts128(sa + box * MN_BOX_BYTES + (valid + (rem >> 3)) * 128 + (rem & 7) * 16, zero);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
           }
         }
-        if (!ok) break;
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            if (kk < ksteps) {
+              // MN-major operands: a K step of 16 is two 8-row groups, 2048 bytes on.
+              const uint64_t adesc = S::a_mn ? ptx::sdesc_mnmajor_sw128(sa + kk * 2048, MN_BOX_BYTES)
+                                             : ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2);
+              const uint64_t bdesc = S::b_mn ? ptx::sdesc_mnmajor_sw128(sb + kk * 2048, MN_BOX_BYTES)
+                                             : ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2);
+              ptx::umma_bf16(d_tmem, adesc, bdesc, S::idesc, (first && kk == 0) ? 0u : 1u);
+            }
+          }
+          ptx::umma_commit(&ctl->empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
         if (nkb > 0) {
           ptx::umma_commit(&ctl->tfull[acc]);
         } else {
           ptx::mbar_arrive(&ctl->tfull[acc]);  // nothing to wait for: the epilogue writes zeros
         }
-        if (++acc == S::n_acc) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
       }
+      __syncwarp();
+      if (++acc == S::n_acc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) {
       ptx::umma_commit(&ctl->drain);
       ptx::mbar_wait(&ctl->drain, 0, nullptr, drain_limit(args.wait_ns));
     }
@@ -421,14 +473,18 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
         const int col0 = n * BNH;
 #pragma unroll 1
         for (int c = 0; c < BNH; c += 32) {
+          const bool live = rows > 0 && col0 + c < args.n_out;
+          const size_t base = static_cast<size_t>(row0) * args.n_out + col0 + c;
+          // dh's loads go out before the accumulator is read.
+          float t[32];
+          warp_load_rows_f32(args.dh + base, args.n_out, live ? rows : 0, lane, t);
           uint32_t av[32], bv[32];
           ptx::tmem_ld_32x32b_x32(t_row + c, av);
           ptx::tmem_ld_32x32b_x32(t_row + BNH + c, bv);
           ptx::tmem_ld_wait();
-          if (rows > 0 && col0 + c < args.n_out) {
-            const size_t base = static_cast<size_t>(row0) * args.n_out + col0 + c;
+          if (live) {
             float g[32];
-            warp_load_f32(stg, args.dh + base, args.n_out, rows, lane, g);
+            warp_transpose_f32(stg, t, lane, g);
             uint32_t pa[16], pb[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -565,14 +621,6 @@ int launch_bwd(const Maps& maps, BwdArgs a, long long max_tiles, const Ctx& c, c
 
 }  // namespace
 
-// Columns of the [channels, padded tokens] layout: every expert's tokens
-// padded to a multiple of 64, rounded up to a multiple of 64 so that the row
-// stride is a multiple of 128 bytes (a tensor map needs multiples of 16).
-size_t bwd_kpad_cols(int Tk, int E) {
-  const size_t cols = static_cast<size_t>(Tk) + static_cast<size_t>(E) * KPAD;
-  return (cols + KPAD - 1) / KPAD * KPAD;
-}
-
 int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2, float* dh,
                   int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s) {
   if (Tk <= 0) return MOE_OK;
@@ -647,12 +695,13 @@ int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const 
   return launch_bwd<MODE_DX>(m, a, max_tiles, c, s);
 }
 
-int launch_bwd_wgrad(const void* At, const void* Bt, const int32_t* offsets, float* dW, int M, int N, int Tk, int E,
+int launch_bwd_wgrad(const void* A, const void* B, const int32_t* offsets, float* dW, int M, int N, int Tk, int E,
                      const Ctx& c, cudaStream_t s) {
   Maps m;
-  const uint64_t kp = bwd_kpad_cols(Tk, E);
-  int rc = make_tmap(&m.a[0], At, kp, static_cast<uint64_t>(M));
-  if (rc == MOE_OK) rc = make_tmap(&m.b[0], Bt, kp, static_cast<uint64_t>(N));
+  // Token-major [Tk, M] and [Tk, N], read MN-major (64 x 64 boxes).
+  const uint64_t rows = static_cast<uint64_t>(Tk > 0 ? Tk : 1);
+  int rc = make_tmap(&m.a[0], A, static_cast<uint64_t>(M), rows, 64);
+  if (rc == MOE_OK) rc = make_tmap(&m.b[0], B, static_cast<uint64_t>(N), rows, 64);
   if (rc != MOE_OK) return rc;
   m.a[1] = m.a[2] = m.a[0];
   m.b[1] = m.b[2] = m.b[0];

@@ -85,7 +85,6 @@ int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1
 int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d,
                    int dff, int E, const Ctx& c, cudaStream_t s);
 // Backward (bf16 activations, fp32 weight gradients).
-size_t bwd_kpad_cols(int Tk, int E);
 int dwg_chunks(int T);
 int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2, float* dh,
                   int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
@@ -93,7 +92,7 @@ int launch_bwd_dsw(const void* x_perm, const float* dh, const int32_t* offsets, 
                    void* dA, void* dB, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const void* W1, const void* W3,
                   void* dx_perm, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
-int launch_bwd_wgrad(const void* At, const void* Bt, const int32_t* offsets, float* dW, int M, int N, int Tk,
+int launch_bwd_wgrad(const void* A, const void* B, const int32_t* offsets, float* dW, int M, int N, int Tk,
                      int E, const Ctx& c, cudaStream_t s);
 cudaError_t launch_route_bwd(const void* dout, const void* y_perm, const int32_t* slot_pos, const float* w,
                              void* dy_perm, void* dout_perm, float* w_perm, float* dl, int T, int d, int k,
@@ -102,9 +101,6 @@ cudaError_t launch_dx_gather(const void* dx_perm, const int32_t* slot_pos, const
                              const void* Wg, void* dx, int T, int d, int E, int k, const Ctx& c, cudaStream_t s);
 cudaError_t launch_dwg(const void* x, const int32_t* idx, const float* dl, float* part, float* dWg, int T, int d,
                        int E, int k, const Ctx& c, cudaStream_t s);
-cudaError_t launch_transpose_batched(const void* src, void* dst, int B, int R, int C, cudaStream_t s);
-cudaError_t launch_transpose_segments(const void* src, const int32_t* offsets, void* dst, int Tk, int C, int Kp,
-                                      int E, cudaStream_t s);
 // int8 weight-only path: per-row int8 codes + fp32 scales, bf16 activations.
 cudaError_t launch_quantize_int8(const void* W, long long rows, int cols, int8_t* q, float* scale,
                                  const Ctx& c, cudaStream_t s);

@@ -246,6 +246,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 
 // The same with B MN-major (bit 16, "transpose B").
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) { return idesc_bf16_f32(M, N) | (1u << 16); }
+// Both operands MN-major (bit 15 transposes A, bit 16 B).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);
+}
 
 }  // namespace ptx
 }  // namespace moe
