@@ -209,9 +209,10 @@ class Layer:
 
 
 class BwdLayer:
-    """The backward of one workload: the forward runs once at set-up with
-    caller scratch (`saved`), then step() runs moe_backward_ws through the C
-    ABI into preallocated gradients."""
+    """The backward of one workload: the training forward (moe_forward_train_ws,
+    which keeps the SwiGLU's local derivatives p and q) runs once at set-up with caller scratch (`saved`),
+    then step() runs moe_backward_ws through the C ABI into preallocated
+    gradients; forward_step() re-runs that training forward."""
 
     def __init__(self, wl, tensors, device):
         from sparse_mixture_experts_50_b300 import binding as B
@@ -221,15 +222,21 @@ class BwdLayer:
         g = {n: v.to(device) for n, v in tensors.items()}
         self.x, self.Wg, self.W1, self.W3, self.W2, self.dout = g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], g["dout"]
         self.saved = B.workspace(T, d, F, E, k, B.MOE_DTYPE_BF16, device=device)
-        B.moe_forward_ws(self.x, self.Wg, self.W1, self.W3, self.W2, k, self.saved)
+        self.out = torch.empty_like(self.x)
+        self.keep = B.keep_buffer(T, F, k, device=device)
+        self.forward_step()
         self.ws = torch.empty(B.moe_backward_workspace_bytes(T, d, F, E, k), dtype=torch.uint8, device=device)
         self.grads = B._grads(self.x, self.Wg, self.W1, self.W3, self.W2, None)
+
+    def forward_step(self):
+        self.B.moe_forward_train_ws(self.x, self.Wg, self.W1, self.W3, self.W2, self.wl.k, self.saved,
+                                    keep=self.keep, out=self.out)
 
     def step(self, ev=None):
         if ev is not None:
             ev[0].record()
         self.B.moe_backward_ws(self.dout, self.x, self.Wg, self.W1, self.W3, self.W2, self.wl.k, self.saved, self.ws,
-                               self.grads)
+                               self.grads, keep=self.keep)
         if ev is not None:
             for e in ev[1:]:
                 e.record()
@@ -292,8 +299,21 @@ def bench_backward(name, shared, args, device, peaks, dist_on):
     ms = sum(step_ms) / len(step_ms)
     flops = wl.T * wl.k * 12 * wl.d * wl.F + wl.T * wl.k * 4 * wl.d * wl.E
     achieved = flops / (ms * 1e-3) / 1e12
+    # The training forward that feeds it (p and q kept), timed the same way.
+    fwd_ms = []
+    for i in range(args.warmup + args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        layer.forward_step()
+        b.record()
+        flush.zero_()
+        if i >= args.warmup:
+            fwd_ms.append((a, b))
+    torch.cuda.synchronize()
+    fwd = sum(a.elapsed_time(b) for a, b in fwd_ms) / len(fwd_ms)
     return {
         "workload": name, "T": wl.T, "tokens_per_s": wl.T / (ms * 1e-3), "ms_per_step": ms,
+        "train_forward_ms": fwd,
         "layer_roofline_frac": achieved / peaks["bf16_tflops"], "bound": "tensor",
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],

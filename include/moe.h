@@ -281,24 +281,43 @@ int moe_forward_w8(const void* x, const void* Wg, const int8_t* W1q, const float
  *   dW2_e = sum dy^T h,  dW1_e = sum da^T x,  dW3_e = sum db^T x,  dWg[i_j] += dl_j x
  * Inputs: dout[T,d] bf16 and the forward's inputs.  `saved` is the scratch
  * that moe_forward_ws(x, Wg, W1, W3, W2, out, ..., MOE_DTYPE_BF16, saved,
- * saved_bytes, ...) filled for the same inputs, unmodified since (it holds
- * the routing, the permutation, x_perm, h and y_perm).  Outputs (overwritten):
+ * saved_bytes, ...) or moe_forward_train_ws filled for the same inputs,
+ * unmodified since (it holds the routing, the permutation, x_perm, h and
+ * y_perm).  `keep` is NULL, or the buffer that moe_forward_train_ws filled
+ * in that same call: then da = dh p and db = dh q come from the kept p and q
+ * instead of a and b recomputed (one GEMM of 4*T*k*d*dff flop less).
+ * Outputs (overwritten):
  * dx[T,d] bf16; dWg[E,d], dW1[E,dff,d], dW3[E,dff,d], dW2[E,d,dff] fp32 (an
  * expert no token chose gets zeros).  dh is formed in fp32 from the exact
  * dout rows and the fp32 gate weight; the intermediates da, db, the permuted
  * dx and (for dW2 only) dy are bf16; every GEMM accumulates in fp32 on the
- * tensor cores.
+ * tensor cores.  Recomputed, a and b are fp32; kept, p and q are formed in
+ * fp32 from the forward's fp32 a and b and rounded once to bf16, which
+ * perturbs da and db by one bf16 rounding relative to themselves (keeping a
+ * itself in bf16 would not: silu'(a) crosses zero near a = -1.28).
  * Shapes as the bf16 forward.  The block form is not differentiated here.
  */
+/*
+ * The training forward: moe_forward_ws in bf16 (same `out`, same scratch
+ * contents) that also keeps, for moe_backward_ws, the local derivatives of
+ * the SwiGLU h = silu(a) b at the gate/up GEMM's a = x W1_e^T, b = x W3_e^T:
+ * p = b silu'(a) and q = silu(a), formed in fp32 and rounded to bf16, in
+ * keep[2][T*k][dff] (device, caller-owned, 16-byte aligned; plane 0 = p,
+ * plane 1 = q, rows in the permuted order of the scratch's x_perm):
+ * 4*T*k*dff bytes.  Errors as moe_forward_ws; keep == NULL is MOE_EINVAL.
+ */
+int moe_forward_train_ws(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
+                         void* out, void* keep, int T, int d, int dff, int E, int k, void* workspace,
+                         size_t workspace_bytes, moe_stream_t stream);
 size_t moe_backward_workspace_bytes(int T, int d, int dff, int E, int k);
 int moe_backward_ws(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3,
-                    const void* W2, const void* saved, size_t saved_bytes, void* dx, float* dWg, float* dW1,
-                    float* dW3, float* dW2, int T, int d, int dff, int E, int k, void* workspace,
-                    size_t workspace_bytes, moe_stream_t stream);
+                    const void* W2, const void* saved, size_t saved_bytes, const void* keep, void* dx,
+                    float* dWg, float* dW1, float* dW3, float* dW2, int T, int d, int dff, int E, int k,
+                    void* workspace, size_t workspace_bytes, moe_stream_t stream);
 /* As moe_backward_ws, scratch from cudaMallocAsync on `stream`. */
 int moe_backward(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
-                 const void* saved, size_t saved_bytes, void* dx, float* dWg, float* dW1, float* dW3, float* dW2,
-                 int T, int d, int dff, int E, int k, moe_stream_t stream);
+                 const void* saved, size_t saved_bytes, const void* keep, void* dx, float* dWg, float* dW1,
+                 float* dW3, float* dW2, int T, int d, int dff, int E, int k, moe_stream_t stream);
 
 /*
  * Scratch size built into moe_forward_noalloc (16 MiB per GPU).

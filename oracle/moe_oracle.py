@@ -114,11 +114,16 @@ def silu(a) -> np.ndarray:
     return a / (1.0 + np.exp(-a))
 
 
+def gate_up_preactivations(x, W1e, W3e):
+    """Section 04, SwiGLUFeedForward: the two projections a = W1 x (gate) and
+    b = W3 x (up) that the SwiGLU combines, each [n,F]."""
+    x = f64(x)
+    return x @ f64(W1e).T, x @ f64(W3e).T
+
+
 def swiglu_hidden(x, W1e, W3e) -> np.ndarray:
     """Section 04, SwiGLUFeedForward: the hidden activation silu(W1 x) * (W3 x), [n,F]."""
-    x = f64(x)
-    a = x @ f64(W1e).T
-    b = x @ f64(W3e).T
+    a, b = gate_up_preactivations(x, W1e, W3e)
     return silu(a) * b
 
 

@@ -56,8 +56,10 @@ SIGNATURES = {
     "moe_forward_w8_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_forward_w8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_backward_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
-    "moe_backward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
-    "moe_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "moe_backward_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ,
+                             _P]),
+    "moe_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "moe_forward_train_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_get_device_status": (_I, [_P, ctypes.POINTER(_I), _I]),
     "moe_set_wait_limit_ns": (_I, [_LL]),
@@ -435,30 +437,54 @@ def _grads(x, Wg, W1, W3, W2, grads):
             "dW2": torch.empty(W2.shape, dtype=torch.float32, device=dev)}
 
 
-def moe_backward_ws(dout, x, Wg, W1, W3, W2, k, saved, ws, grads=None, stream=None):
+def keep_buffer(T, dff, k, device="cuda"):
+    """The bf16 [2, T*k, dff] buffer moe_forward_train_ws fills with
+    p = b silu'(a) (plane 0) and q = silu(a) (plane 1)."""
+    return torch.empty((2, T * k, dff), dtype=torch.bfloat16, device=device)
+
+
+def moe_forward_train_ws(x, Wg, W1, W3, W2, k, ws, keep=None, out=None, stream=None):
+    """The bf16 layer on caller scratch `ws` that also keeps p and q for the
+    backward: returns (out[T,d], keep[2,T*k,dff])."""
+    _dev(x, Wg, W1, W3, W2, ws, out, keep)
+    T, d = x.shape
+    E, dff, _ = W1.shape
+    if keep is None:
+        keep = keep_buffer(T, dff, k, device=x.device)
+    if out is None:
+        out = torch.empty_like(x)
+    _check("moe_forward_train_ws", lib().moe_forward_train_ws(_p(x), _p(Wg), _p(W1), _p(W3), _p(W2), _p(out),
+                                                              _p(keep), T, d, dff, E, k, _p(ws), ws.numel(),
+                                                              _stream(stream)))
+    return out, keep
+
+
+def moe_backward_ws(dout, x, Wg, W1, W3, W2, k, saved, ws, grads=None, stream=None, keep=None):
     """Backward of the bf16 layer.  `saved` is the uint8 scratch the forward
-    (moe_forward_ws) used on the same inputs; `ws` the backward's scratch.
-    Returns dict(dx, dWg, dW1, dW3, dW2)."""
-    _dev(dout, x, Wg, W1, W3, W2, saved, ws)
+    (moe_forward_ws or moe_forward_train_ws) used on the same inputs; `keep`
+    None or the p/q buffer of that moe_forward_train_ws call; `ws` the
+    backward's scratch.  Returns dict(dx, dWg, dW1, dW3, dW2)."""
+    _dev(dout, x, Wg, W1, W3, W2, saved, ws, keep)
     T, d = x.shape
     E, dff, _ = W1.shape
     g = _grads(x, Wg, W1, W3, W2, grads)
     _check("moe_backward_ws", lib().moe_backward_ws(_p(dout), _p(x), _p(Wg), _p(W1), _p(W3), _p(W2), _p(saved),
-                                                    saved.numel(), _p(g["dx"]), _p(g["dWg"]), _p(g["dW1"]),
-                                                    _p(g["dW3"]), _p(g["dW2"]), T, d, dff, E, k, _p(ws), ws.numel(),
-                                                    _stream(stream)))
+                                                    saved.numel(), _p(keep), _p(g["dx"]), _p(g["dWg"]),
+                                                    _p(g["dW1"]), _p(g["dW3"]), _p(g["dW2"]), T, d, dff, E, k,
+                                                    _p(ws), ws.numel(), _stream(stream)))
     return g
 
 
-def moe_backward(dout, x, Wg, W1, W3, W2, k, saved, grads=None, stream=None):
+def moe_backward(dout, x, Wg, W1, W3, W2, k, saved, grads=None, stream=None, keep=None):
     """As moe_backward_ws with scratch from the stream-ordered pool."""
-    _dev(dout, x, Wg, W1, W3, W2, saved)
+    _dev(dout, x, Wg, W1, W3, W2, saved, keep)
     T, d = x.shape
     E, dff, _ = W1.shape
     g = _grads(x, Wg, W1, W3, W2, grads)
     _check("moe_backward", lib().moe_backward(_p(dout), _p(x), _p(Wg), _p(W1), _p(W3), _p(W2), _p(saved),
-                                              saved.numel(), _p(g["dx"]), _p(g["dWg"]), _p(g["dW1"]), _p(g["dW3"]),
-                                              _p(g["dW2"]), T, d, dff, E, k, _stream(stream)))
+                                              saved.numel(), _p(keep), _p(g["dx"]), _p(g["dWg"]),
+                                              _p(g["dW1"]), _p(g["dW3"]), _p(g["dW2"]), T, d, dff, E, k,
+                                              _stream(stream)))
     return g
 
 

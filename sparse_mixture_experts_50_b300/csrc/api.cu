@@ -108,8 +108,8 @@ int check_ffn(int Tk, int d, int dff, int E, int dtype) {
 }
 
 int ffn_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, void* h, int Tk, int d,
-                int dff, int E, int dtype, const Ctx& c, cudaStream_t s) {
-  if (dtype == MOE_DTYPE_BF16) return launch_tc_gate_up(x_perm, offsets, W1, W3, h, Tk, d, dff, E, c, s);
+                int dff, int E, int dtype, const Ctx& c, cudaStream_t s, void* keep = nullptr) {
+  if (dtype == MOE_DTYPE_BF16) return launch_tc_gate_up(x_perm, offsets, W1, W3, h, Tk, d, dff, E, c, s, keep);
   return launch_rc(launch_ffn_f32_gate_up(static_cast<const float*>(x_perm), offsets, static_cast<const float*>(W1),
                                           static_cast<const float*>(W3), static_cast<float*>(h), Tk, d, dff, E, c, s));
 }
@@ -160,9 +160,13 @@ WsLayout ws_layout(int T, int d, int dff, int E, int k, int dtype) {
 // NULL the int8 expert weights (W1, W3, W2 are then unused).
 // `events` (optional, 5 caller-created cudaEvent_t) are recorded before the
 // router, after dispatch, after gate/up, after down and after combine.
+// `keep` (optional, bf16 only) receives p = b silu'(a) and q = silu(a) of the
+// gate/up GEMM's a and b in bf16, planes [2, T*k, dff] in the permuted row
+// order, for the backward.
 int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, const void* W1, const void* W3,
                  const void* W2, void* out, int T, int d, int dff, int E, int k, int dtype, void* ws, size_t ws_bytes,
-                 const Ctx& cin, cudaStream_t s, const W8Weights* w8 = nullptr, void* const* events = nullptr) {
+                 const Ctx& cin, cudaStream_t s, const W8Weights* w8 = nullptr, void* const* events = nullptr,
+                 void* keep = nullptr) {
   Ctx c = cin;
   c.max_rows_per_expert = T;  // each token picks an expert at most once
   auto mark = [&](int i) -> int {
@@ -198,7 +202,7 @@ int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, co
     MOE_TRY(mark(2));
     MOE_TRY(launch_w8_down(h, offs, w8->q2, w8->s2, y, Tk, d, dff, E, c, s));
   } else {
-    MOE_TRY(ffn_gate_up(x_perm, offs, W1, W3, h, Tk, d, dff, E, dtype, c, s));
+    MOE_TRY(ffn_gate_up(x_perm, offs, W1, W3, h, Tk, d, dff, E, dtype, c, s, keep));
     MOE_TRY(mark(2));
     MOE_TRY(ffn_down(h, offs, W2, y, Tk, d, dff, E, dtype, c, s));
   }
@@ -302,8 +306,8 @@ BwdLayout bwd_layout(int T, int d, int dff, int E, int k) {
 // The backward, B1..B7, on caller scratch; `saved` is the scratch of the
 // forward call (moe_forward_ws) on the same x and weights.
 int backward_impl(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
-                  const void* saved, void* dx, float* dWg, float* dW1, float* dW3, float* dW2, int T, int d, int dff,
-                  int E, int k, void* ws, const Ctx& c, cudaStream_t s) {
+                  const void* saved, const void* keep, void* dx, float* dWg, float* dW1, float* dW3, float* dW2,
+                  int T, int d, int dff, int E, int k, void* ws, const Ctx& c, cudaStream_t s) {
   const WsLayout F = ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16);
   const BwdLayout L = bwd_layout(T, d, dff, E, k);
   const uint8_t* sv = static_cast<const uint8_t*>(saved);
@@ -325,10 +329,15 @@ int backward_impl(const void* dout, const void* x, const void* Wg, const void* W
   const int Tk = T * k;
   // B1-B2: expert-output and gate-weight gradients, softmax over the k chosen.
   MOE_TRY(launch_rc(launch_route_bwd(dout, y_perm, slot_pos, w, dy, dop, wp, dl, T, d, k, c, s)));
-  // B3: dh = w (dout W2) in fp32; a and b recomputed, SwiGLU derivative -> dA, dB.
+  // B3: dh = w (dout W2) in fp32 and the SwiGLU derivative -> dA, dB: from
+  // the p and q the training forward kept, else with a and b recomputed.
   float* dh = reinterpret_cast<float*>(b + L.dh);
-  MOE_TRY(launch_bwd_dh(dop, wp, offs, W2, dh, Tk, d, dff, E, c, s));
-  MOE_TRY(launch_bwd_dsw(x_perm, dh, offs, W1, W3, dA, dB, Tk, d, dff, E, c, s));
+  if (keep != nullptr) {
+    MOE_TRY(launch_bwd_dh(dop, wp, offs, W2, nullptr, keep, dA, dB, Tk, d, dff, E, c, s));
+  } else {
+    MOE_TRY(launch_bwd_dh(dop, wp, offs, W2, dh, nullptr, nullptr, nullptr, Tk, d, dff, E, c, s));
+    MOE_TRY(launch_bwd_dsw(x_perm, dh, offs, W1, W3, dA, dB, Tk, d, dff, E, c, s));
+  }
   // B4: dx_perm = dA W1 + dB W3.
   MOE_TRY(launch_bwd_dx(dA, dB, offs, W1, W3, dxp, Tk, d, dff, E, c, s));
   // B5: un-permute + router path -> dx.
@@ -344,8 +353,8 @@ int backward_impl(const void* dout, const void* x, const void* Wg, const void* W
 }
 
 int check_backward(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
-                   const void* saved, size_t saved_bytes, const void* dx, const float* dWg, const float* dW1,
-                   const float* dW3, const float* dW2, int T, int d, int dff, int E, int k) {
+                   const void* saved, size_t saved_bytes, const void* keep, const void* dx, const float* dWg,
+                   const float* dW1, const float* dW3, const float* dW2, int T, int d, int dff, int E, int k) {
   MOE_TRY(check_forward(x, Wg, W1, W3, W2, dx, T, d, dff, E, k, MOE_DTYPE_BF16));
   if (T == 0) return MOE_OK;
   if (static_cast<long long>(E) * dff * d > INT_MAX || static_cast<long long>(T) * k * dff > (1LL << 40))
@@ -354,6 +363,7 @@ int check_backward(const void* dout, const void* x, const void* Wg, const void* 
   for (const void* p : ptrs)
     if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
   if (!aligned(saved, 256)) return MOE_EINVAL;
+  if (keep != nullptr && !aligned(keep, 16)) return MOE_EINVAL;
   if (saved_bytes < ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16).total) return MOE_ENOMEM;
   return MOE_OK;
 }
@@ -495,6 +505,19 @@ int moe_forward_ws(const void* x, const void* Wg, const void* W1, const void* W3
                       stream);
 }
 
+int moe_forward_train_ws(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2, void* out,
+                         void* keep, int T, int d, int dff, int E, int k, void* workspace,
+                         size_t workspace_bytes, moe_stream_t stream) {
+  MOE_TRY(check_forward(x, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_BF16));
+  if (T == 0) return MOE_OK;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
+  if (keep == nullptr || !aligned(keep, 16)) return MOE_EINVAL;
+  Ctx c;
+  MOE_TRY(make_ctx(out, &c));
+  return forward_impl(x, nullptr, 0.0f, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_BF16, workspace,
+                      workspace_bytes, c, stream, nullptr, nullptr, keep);
+}
+
 int moe_forward(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2, void* out, int T, int d,
                 int dff, int E, int k, moe_stream_t stream) {
   return forward_alloc(x, nullptr, 0.0f, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_BF16, stream);
@@ -630,22 +653,25 @@ size_t moe_backward_workspace_bytes(int T, int d, int dff, int E, int k) {
 }
 
 int moe_backward_ws(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
-                    const void* saved, size_t saved_bytes, void* dx, float* dWg, float* dW1, float* dW3, float* dW2,
-                    int T, int d, int dff, int E, int k, void* workspace, size_t workspace_bytes,
-                    moe_stream_t stream) {
-  MOE_TRY(check_backward(dout, x, Wg, W1, W3, W2, saved, saved_bytes, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k));
+                    const void* saved, size_t saved_bytes, const void* keep, void* dx, float* dWg, float* dW1,
+                    float* dW3, float* dW2, int T, int d, int dff, int E, int k, void* workspace,
+                    size_t workspace_bytes, moe_stream_t stream) {
+  MOE_TRY(check_backward(dout, x, Wg, W1, W3, W2, saved, saved_bytes, keep, dx, dWg, dW1, dW3, dW2, T, d, dff, E,
+                         k));
   if (T == 0) return MOE_OK;
   if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
   if (workspace_bytes < bwd_layout(T, d, dff, E, k).total) return MOE_ENOMEM;
   Ctx c;
   MOE_TRY(make_ctx(dx, &c));
-  return backward_impl(dout, x, Wg, W1, W3, W2, saved, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k, workspace, c, stream);
+  return backward_impl(dout, x, Wg, W1, W3, W2, saved, keep, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k, workspace,
+                       c, stream);
 }
 
 int moe_backward(const void* dout, const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
-                 const void* saved, size_t saved_bytes, void* dx, float* dWg, float* dW1, float* dW3, float* dW2,
-                 int T, int d, int dff, int E, int k, moe_stream_t stream) {
-  MOE_TRY(check_backward(dout, x, Wg, W1, W3, W2, saved, saved_bytes, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k));
+                 const void* saved, size_t saved_bytes, const void* keep, void* dx, float* dWg, float* dW1,
+                 float* dW3, float* dW2, int T, int d, int dff, int E, int k, moe_stream_t stream) {
+  MOE_TRY(check_backward(dout, x, Wg, W1, W3, W2, saved, saved_bytes, keep, dx, dWg, dW1, dW3, dW2, T, d, dff, E,
+                         k));
   if (T == 0) return MOE_OK;
   Ctx c;
   MOE_TRY(make_ctx(dx, &c));
@@ -655,7 +681,8 @@ int moe_backward(const void* dout, const void* x, const void* Wg, const void* W1
     cudaGetLastError();
     return MOE_ENOMEM;
   }
-  const int rc = backward_impl(dout, x, Wg, W1, W3, W2, saved, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k, ws, c, stream);
+  const int rc =
+      backward_impl(dout, x, Wg, W1, W3, W2, saved, keep, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k, ws, c, stream);
   const cudaError_t fe = cudaFreeAsync(ws, stream);
   if (rc != MOE_OK) return rc;
   return fe == cudaSuccess ? MOE_OK : MOE_ECUDA;

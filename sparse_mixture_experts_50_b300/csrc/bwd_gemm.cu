@@ -6,6 +6,9 @@
 //   dh = w_p (dout W2_e)                                           (DH, fp32)
 //   a = x W1_e^T,  b = x W3_e^T,
 //   da = dh * b * silu'(a),  db = dh * silu(a)                     (DSW)
+//   When the forward kept p = b silu'(a) and q = silu(a) (bf16, formed from
+//   its fp32 a and b), DH's epilogue forms da = dh p and db = dh q from its
+//   fp32 dh directly and DSW does not run.
 //   dx_perm = da W1_e + db W3_e                                    (DX)
 //   dW2_e = dy^T h,  dW1_e = da^T x,  dW3_e = db^T x               (WGRAD)
 //
@@ -24,7 +27,9 @@
 //   DH       tile 128 rows x 256 h columns, one K=d pass; the epilogue
 //            scales by w_p and stores fp32 (dout is gathered exactly and dh
 //            stays fp32: a bf16 rounding of w dout or of dh would be
-//            amplified by the 4096-term sum where it cancels).
+//            amplified by the 4096-term sum where it cancels), or, given
+//            the kept p and q, reads them (one 32-column chunk ahead) and
+//            stores da, db in bf16.
 //   DSW      tile 128 rows x 128 h columns: a and b recomputed in one K=d
 //            pass over the W1 and W3 rows (N=256, as the forward's gate/up
 //            GEMM); the epilogue reads dh, forms da, db in fp32 and rounds
@@ -80,8 +85,10 @@ struct Ctl {
 constexpr int STG_PITCH = 33;             // staging block row pitch (32-bit words)
 constexpr int STG_WORDS = 32 * STG_PITCH;  // one warp's staging block
 constexpr size_t CTL_BYTES = (sizeof(Ctl) + 15) / 16 * 16;
-constexpr size_t SMEM_BYTES =
-    1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + CTL_BYTES + 4 * STG_WORDS * sizeof(uint32_t);
+constexpr int KEEP_WORDS = 2 * 32 * 16;    // DH: one warp's p and q chunk (32 rows x 32 bf16 each)
+constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + CTL_BYTES +
+                              4 * STG_WORDS * sizeof(uint32_t) + 4 * KEEP_WORDS * sizeof(uint32_t);
+static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 
 struct BwdArgs {
   const int32_t* offsets;  // [E+1] routed-row boundaries
@@ -99,6 +106,7 @@ struct BwdArgs {
   float* outf;             // WGRAD: [E, M, N]; DH: dh [Tk, F]
   const float* w_perm;     // DH: gate weight of each routed row [Tk]
   const float* dh;         // DSW: dh [Tk, F] fp32
+  const __nv_bfloat16* keep;  // DH, optional: the forward's p, q planes [2, Tk, F]
   int* status;
   unsigned long long wait_ns;
 };
@@ -159,6 +167,40 @@ __device__ __forceinline__ void warp_transpose_f32(uint32_t* stg, const float (&
   __syncwarp();
 }
 
+// Rows r < rows of a bf16 src (row stride ld, 32 columns each): t[i] holds
+// row 2i + lane/16, columns 2(lane%16), +1 (two 64-byte rows per
+// instruction); rows past `rows` read as zero.
+__device__ __forceinline__ void warp_load_rows_bf16(const __nv_bfloat16* src, size_t ld, int rows, int lane,
+                                                    uint32_t (&t)[16]) {
+  const int half = lane >> 4, w = lane & 15;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int r = 2 * i + half;
+    t[i] = r < rows ? __ldg(reinterpret_cast<const unsigned int*>(src + r * ld) + w) : 0u;
+  }
+}
+
+// The transpose of what warp_load_rows_bf16 read: lane = row, pk[i] =
+// columns 2i, 2i+1.
+__device__ __forceinline__ void warp_transpose_bf16(uint32_t* stg, const uint32_t (&t)[16], int lane,
+                                                    uint32_t (&pk)[16]) {
+  const int half = lane >> 4, w = lane & 15;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) stg[(2 * i + half) * 17 + w] = t[i];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = stg[lane * 17 + i];
+  __syncwarp();
+}
+
+// The SwiGLU derivative for h = silu(a) b, given dh = g:
+// da = g b silu'(a) with silu'(a) = s (1 + a (1 - s)), s = sigmoid(a); db = g silu(a).
+__device__ __forceinline__ void swiglu_grad(float g, float a, float b, float& da, float& db) {
+  const float s = __frcp_rn(1.0f + __expf(-a));  // = 1.0f / (1 + e^-a), correctly rounded
+  da = g * b * (s * (1.0f + a * (1.0f - s)));
+  db = g * (a * s);
+}
+
 // The warp's 32 rows x 32 bf16 columns (lane = row, pk[i] = columns 2i,
 // 2i+1) to dst[r * ld + ...] for r < rows: two 64-byte rows per instruction.
 __device__ __forceinline__ void warp_store_bf16(uint32_t* stg, const uint32_t (&pk)[16], __nv_bfloat16* dst,
@@ -202,6 +244,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
   uint32_t* stage_blocks = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES + CTL_BYTES);
+  uint32_t* keep_blocks = stage_blocks + 4 * STG_WORDS;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const volatile int* abort_flag = &ctl->abort_flag;
@@ -438,9 +481,28 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
     const int quad = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // DH with the kept p and q: each lane asks L2 for its row of a tile's p
+    // and q one tile ahead, so that the epilogue's loads hit L2.
+    auto prefetch_keep = [&](int t) {
+      if (MODE != MODE_DH || args.keep == nullptr || t >= total_tiles) return;
+      int pe, pm, pn;
+      decode_tile(ctl, args.E, t, pe, pm, pn);
+      const int prow0 = ctl->seg[pe] + pm * BM + quad * 32;
+      const int prows = max(0, min(32, ctl->seg[pe + 1] - prow0));
+      const int pcol0 = pn * 2 * BNH;
+      const int ncols = min(2 * BNH, args.n_out - pcol0);
+      if (lane < prows && ncols > 0) {
+        const size_t o = static_cast<size_t>(prow0 + lane) * args.n_out + pcol0;
+        ptx::prefetch_l2_bulk(args.keep + o, static_cast<uint32_t>(ncols) * 2u);
+        ptx::prefetch_l2_bulk(args.keep + static_cast<size_t>(args.Tk) * args.n_out + o,
+                              static_cast<uint32_t>(ncols) * 2u);
+      }
+    };
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int e, m, n;
       decode_tile(ctl, args.E, tile, e, m, n);
+      if (tile == blockIdx.x) prefetch_keep(tile);
+      prefetch_keep(tile + gridDim.x);
       const bool ready = ptx::mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag, args.wait_ns);
       if (!__all_sync(0xFFFFFFFFu, ready)) {
         raise_abort(ctl, args.status);
@@ -455,6 +517,62 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
         const int rows = max(0, min(32, ctl->seg[e + 1] - row0));
         const int col0 = n * 2 * BNH;
         const float wp = lane < rows ? __ldg(args.w_perm + row0 + lane) : 0.0f;
+        if (args.keep != nullptr) {
+          // dh stays in registers: da = dh p, db = dh q.  The p and q rows of
+          // the next 32-column chunk are copied asynchronously into the
+          // warp's keep block while this chunk is worked on; word w of row r
+          // sits at r*16 + (w ^ (r & 15)), so the transposed reads (lane =
+          // row) meet at most two lanes per bank.
+          uint32_t* kb = keep_blocks + quad * KEEP_WORDS;
+          const uint32_t kb_s = ptx::smem_u32(kb);
+          const __nv_bfloat16* qplane = args.keep + static_cast<size_t>(args.Tk) * args.n_out;
+          const size_t rbase = static_cast<size_t>(row0) * args.n_out + col0;
+          const int half = lane >> 4, w = lane & 15;
+          auto issue = [&](int c) {
+            const int lr = (rows > 0 && col0 + c < args.n_out) ? rows : 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int r = 2 * i + half;
+              const bool ok = r < lr;
+              const size_t off = ok ? rbase + static_cast<size_t>(r) * args.n_out + c + 2 * w : 0;
+              const uint32_t dst = kb_s + static_cast<uint32_t>(r * 16 + (w ^ (r & 15))) * 4u;
+              ptx::cp_async_4(dst, args.keep + off, ok ? 4u : 0u);
+              ptx::cp_async_4(dst + 32 * 16 * 4, qplane + off, ok ? 4u : 0u);
+            }
+            ptx::cp_async_commit();
+          };
+          issue(0);
+#pragma unroll 1
+          for (int c = 0; c < 2 * BNH; c += 32) {
+            const bool live = rows > 0 && col0 + c < args.n_out;
+            ptx::cp_async_wait_all();
+            __syncwarp();
+            uint32_t pa[16], pb[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              pa[i] = kb[lane * 16 + (i ^ (lane & 15))];
+              pb[i] = kb[32 * 16 + lane * 16 + (i ^ (lane & 15))];
+            }
+            __syncwarp();
+            if (c + 32 < 2 * BNH) issue(c + 32);
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(t_row + c, v);
+            ptx::tmem_ld_wait();
+            if (live) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[i]));
+                const float2 q2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb[i]));
+                const float g0 = wp * __uint_as_float(v[2 * i]);
+                const float g1 = wp * __uint_as_float(v[2 * i + 1]);
+                pa[i] = pack_bf16x2(g0 * p2.x, g1 * p2.y);
+                pb[i] = pack_bf16x2(g0 * q2.x, g1 * q2.y);
+              }
+              warp_store_bf16(stg, pa, args.out0 + rbase + c, args.n_out, rows, lane);
+              warp_store_bf16(stg, pb, args.out1 + rbase + c, args.n_out, rows, lane);
+            }
+          }
+        } else {
 #pragma unroll 1
         for (int c = 0; c < 2 * BNH; c += 32) {
           uint32_t v[32];
@@ -466,6 +584,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
             warp_store_f32(stg, v, args.outf + static_cast<size_t>(row0) * args.n_out + col0 + c, args.n_out, rows,
                            lane);
           }
+        }
         }
       } else if (MODE == MODE_DSW) {
         const int row0 = ctl->seg[e] + m * BM + quad * 32;
@@ -490,13 +609,8 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
             for (int i = 0; i < 16; ++i) {
               float da[2], db[2];
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const float a = __uint_as_float(av[2 * i + h]);
-                const float b = __uint_as_float(bv[2 * i + h]);
-                const float s = 1.0f / (1.0f + __expf(-a));
-                da[h] = g[2 * i + h] * b * (s * (1.0f + a * (1.0f - s)));
-                db[h] = g[2 * i + h] * (a * s);
-              }
+              for (int h = 0; h < 2; ++h)
+                swiglu_grad(g[2 * i + h], __uint_as_float(av[2 * i + h]), __uint_as_float(bv[2 * i + h]), da[h], db[h]);
               pa[i] = pack_bf16x2(da[0], da[1]);
               pb[i] = pack_bf16x2(db[0], db[1]);
             }
@@ -622,7 +736,8 @@ int launch_bwd(const Maps& maps, BwdArgs a, long long max_tiles, const Ctx& c, c
 }  // namespace
 
 int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2, float* dh,
-                  int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s) {
+                  const void* keep, void* dA, void* dB, int Tk, int d, int dff, int E, const Ctx& c,
+                  cudaStream_t s) {
   if (Tk <= 0) return MOE_OK;
   Maps m;
   int rc = make_tmap(&m.a[0], dout_perm, d, Tk);
@@ -641,6 +756,9 @@ int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* off
   a.n_tiles = (dff + 2 * BNH - 1) / (2 * BNH);
   a.outf = dh;
   a.w_perm = w_perm;
+  a.keep = static_cast<const __nv_bfloat16*>(keep);
+  a.out0 = static_cast<__nv_bfloat16*>(dA);
+  a.out1 = static_cast<__nv_bfloat16*>(dB);
   const long long max_tiles = (static_cast<long long>(Tk) / BM + (E < Tk ? E : Tk)) * a.n_tiles;
   return launch_bwd<MODE_DH>(m, a, max_tiles, c, s);
 }

@@ -185,6 +185,8 @@ struct GemmArgs {
   __nv_bfloat16* out;      // [Tk, ldo]
   const float* scale0;     // int8 path: row scales of B0 [E * b_rows]
   const float* scale1;     // int8 path: row scales of B1 (gate/up only)
+  __nv_bfloat16* keep;     // bf16 gate/up, optional (training): the SwiGLU's
+                           // local derivatives, planes [2, Tk, ldo] (see keep_pair)
   int ldo;                 // row stride of out (elements)
   int n_out;               // valid output columns
   int b_rows;              // rows per expert in the B tensor(s)
@@ -251,6 +253,17 @@ __device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_
   lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
   hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
 #endif
+}
+
+// What the training forward keeps for the backward of h = silu(a) b, formed
+// in fp32 from the GEMM's fp32 a and b and rounded once to bf16:
+// p = dh/da / dh = b silu'(a) = b s (1 + a (1 - s)) and q = dh/db / dh =
+// silu(a) = a s, with s = sigmoid(a).  The backward then needs only
+// da = dh p and db = dh q.
+__device__ __forceinline__ void keep_pair(float a, float b, float& p, float& q) {
+  const float s = __frcp_rn(1.0f + __expf(-a));
+  q = a * s;
+  p = b * (s * (1.0f + a * (1.0f - s)));
 }
 
 template <bool SWIGLU, bool W8, bool SWAP>
@@ -502,7 +515,17 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
             for (int j = 0; j < TN; ++j) {
               if (j < rows_here) {
                 float v = s0 * __uint_as_float(a[j]);
-                if (SWIGLU) v = v / (1.0f + __expf(-v)) * (s1 * __uint_as_float(b[j]));
+                if (SWIGLU) {
+                  const float u = s1 * __uint_as_float(b[j]);
+                  if (!W8 && args.keep != nullptr) {
+                    const size_t o = (static_cast<size_t>(row0) + j) * args.ldo + col;
+                    float pp, qq;
+                    keep_pair(v, u, pp, qq);
+                    args.keep[o] = __float2bfloat16_rn(pp);
+                    args.keep[static_cast<size_t>(args.Tk) * args.ldo + o] = __float2bfloat16_rn(qq);
+                  }
+                  v = v / (1.0f + __expf(-v)) * u;
+                }
                 dst[static_cast<size_t>(j) * args.ldo] = __float2bfloat16_rn(v);
               }
             }
@@ -538,6 +561,25 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
             uint4* dst = reinterpret_cast<uint4*>(args.out + static_cast<size_t>(grow) * args.ldo + col0 + c);
 #pragma unroll
             for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            if (!W8 && args.keep != nullptr) {
+              // The training forward also keeps p and q (keep_pair) for the backward.
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float p0, q0, p1, q1;
+                keep_pair(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), p0, q0);
+                keep_pair(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]), p1, q1);
+                g[i] = pack_bf16x2(p0, p1);
+                u[i] = pack_bf16x2(q0, q1);
+              }
+              const size_t o = static_cast<size_t>(grow) * args.ldo + col0 + c;
+              uint4* dp = reinterpret_cast<uint4*>(args.keep + o);
+              uint4* dq = reinterpret_cast<uint4*>(args.keep + static_cast<size_t>(args.Tk) * args.ldo + o);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                dp[q] = make_uint4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+                dq[q] = make_uint4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+              }
+            }
           }
         }
       } else {
@@ -844,11 +886,12 @@ int launch_mode(const void* A, const void* B0, const void* B1, GemmArgs a, const
 template <bool SWIGLU, bool W8>
 int launch_gemm(const void* A, const void* B0, const void* B1, const float* S0, const float* S1,
                 const int32_t* offsets, void* out, int Tk, int K, int n_out, int b_rows, int E, const Ctx& c,
-                cudaStream_t s) {
+                cudaStream_t s, void* keep = nullptr) {
   if (Tk <= 0) return MOE_OK;
   GemmArgs a;
   a.offsets = offsets;
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.keep = static_cast<__nv_bfloat16*>(keep);
   a.scale0 = S0;
   a.scale1 = S1;
   a.ldo = n_out;
@@ -868,8 +911,8 @@ int launch_gemm(const void* A, const void* B0, const void* B1, const float* S0, 
 }  // namespace
 
 int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, void* h, int Tk,
-                      int d, int dff, int E, const Ctx& c, cudaStream_t s) {
-  return launch_gemm<true, false>(x_perm, W1, W3, nullptr, nullptr, offsets, h, Tk, d, dff, dff, E, c, s);
+                      int d, int dff, int E, const Ctx& c, cudaStream_t s, void* keep) {
+  return launch_gemm<true, false>(x_perm, W1, W3, nullptr, nullptr, offsets, h, Tk, d, dff, dff, E, c, s, keep);
 }
 
 int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d, int dff, int E,

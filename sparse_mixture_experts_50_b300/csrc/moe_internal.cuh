@@ -80,14 +80,18 @@ cudaError_t launch_ffn_f32_gate_up(const float* x_perm, const int32_t* offsets, 
 cudaError_t launch_ffn_f32_down(const float* h, const int32_t* offsets, const float* W2, float* y,
                                 int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 // bf16 tcgen05 path; returns MOE_* status (tensor-map encoding can fail).
+// keep (optional): bf16 planes [2, Tk, dff] of p = b silu'(a) and
+// q = silu(a), for the backward.
 int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3,
-                      void* h, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
+                      void* h, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s, void* keep = nullptr);
 int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d,
                    int dff, int E, const Ctx& c, cudaStream_t s);
 // Backward (bf16 activations, fp32 weight gradients).
 int dwg_chunks(int T);
+// keep == NULL: dh (fp32) to `dh`; else the forward's p and q ([2, Tk, dff]
+// bf16) give da = dh p, db = dh q (bf16) to dA, dB directly.
 int launch_bwd_dh(const void* dout_perm, const float* w_perm, const int32_t* offsets, const void* W2, float* dh,
-                  int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
+                  const void* keep, void* dA, void* dB, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 int launch_bwd_dsw(const void* x_perm, const float* dh, const int32_t* offsets, const void* W1, const void* W3,
                    void* dA, void* dB, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 int launch_bwd_dx(const void* dA, const void* dB, const int32_t* offsets, const void* W1, const void* W3,

@@ -50,17 +50,24 @@ def seeded_dout(T, d, seed):
 
 
 def run_gpu(B, t, k, dout, entry="alloc"):
+    """entry: "alloc" / "ws" = moe_backward / moe_backward_ws after
+    moe_forward_ws (a and b recomputed); "keep" / "ws_keep" the same after
+    moe_forward_train_ws, with its kept a and b."""
     g = {n: v.to(DEV).contiguous() for n, v in t.items()}
     T, d = g["x"].shape
     E, F, _ = g["W1"].shape
     saved = B.workspace(T, d, F, E, k, B.MOE_DTYPE_BF16)
-    B.moe_forward_ws(g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved)
-    dd = dout.to(DEV)
-    if entry == "ws":
-        ws = torch.empty(B.moe_backward_workspace_bytes(T, d, F, E, k), dtype=torch.uint8, device=DEV)
-        grads = B.moe_backward_ws(dd, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved, ws)
+    keep = None
+    if entry.endswith("keep"):
+        _, keep = B.moe_forward_train_ws(g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved)
     else:
-        grads = B.moe_backward(dd, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved)
+        B.moe_forward_ws(g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved)
+    dd = dout.to(DEV)
+    if entry.startswith("ws"):
+        ws = torch.empty(B.moe_backward_workspace_bytes(T, d, F, E, k), dtype=torch.uint8, device=DEV)
+        grads = B.moe_backward_ws(dd, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved, ws, keep=keep)
+    else:
+        grads = B.moe_backward(dd, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved, keep=keep)
     status_ok(B)
     v = B.workspace_views(saved, T, d, F, E, k)
     return grads, v["idx"].cpu().numpy(), v["w"].cpu().numpy()
@@ -75,7 +82,7 @@ def oracle_grads(t, k, dout, gidx, gw, experts=None):
 
 
 @pytest.mark.parametrize("name", ["small_bf16", "small_ragged", "small_skewed_zero"])
-@pytest.mark.parametrize("entry", ["alloc", "ws"])
+@pytest.mark.parametrize("entry", ["alloc", "ws", "keep", "ws_keep"])
 def test_backward_small(B, name, entry):
     wl = mw.get(name)
     t = mw.make_inputs(wl)
@@ -104,13 +111,14 @@ def test_backward_linear_in_dout(B):
         assert torch.equal(g2[n], 2 * g1[n]), n
 
 
-def test_backward_mixtral_shape(B):
+@pytest.mark.parametrize("entry", ["alloc", "keep"])
+def test_backward_mixtral_shape(B, entry):
     """Mixtral sizes (d=4096, d_ff=14336, E=8, top-2) at 64 tokens: dx and dWg
     in full, the expert weight gradients of two experts."""
     wl = mw.get("decode").with_tokens(64)
     t = mw.make_inputs(wl)
     dout = seeded_dout(wl.T, wl.d, 9)
-    grads, gidx, gw = run_gpu(B, t, wl.k, dout)
+    grads, gidx, gw = run_gpu(B, t, wl.k, dout, entry)
     counts = np.bincount(gidx.ravel(), minlength=wl.E)
     pick = [int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))]
     ref, _ = oracle_grads(t, wl.k, dout, gidx, gw, experts=pick)
@@ -119,3 +127,39 @@ def test_backward_mixtral_shape(B):
     for e in pick:
         for n in ("dW1", "dW3", "dW2"):
             check_backward_close(to_np(grads[n][e]), ref[n][e], ref[n + "_scale"][e], f"mixtral {n}[{e}]")
+
+
+@pytest.mark.parametrize("name", ["small_ragged", "decode"])
+def test_forward_train_keeps_swiglu_derivatives(B, name):
+    """moe_forward_train_ws: the same output and scratch as moe_forward_ws
+    (bit for bit: the same kernels), plus the SwiGLU's local derivatives of
+    every permuted row in bf16, p = b silu'(a) and q = silu(a) at
+    a = x W1_e^T, b = x W3_e^T, checked against the oracle's fp64 values with
+    the bf16 forward tolerance.  "decode" (T=1) runs the small-batch GEMM
+    form, small_ragged the tiled one."""
+    from parity import check_close
+    wl = mw.get(name)
+    t = mw.make_inputs(wl)
+    g = {n: v.to(DEV).contiguous() for n, v in t.items()}
+    T, d, F, E, k = wl.T, wl.d, wl.F, wl.E, wl.k
+    ws1 = B.workspace(T, d, F, E, k)
+    ws2 = B.workspace(T, d, F, E, k)
+    ws1.zero_()
+    ws2.zero_()
+    out1 = B.moe_forward_ws(g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, ws1)
+    out2, keep = B.moe_forward_train_ws(g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, ws2)
+    status_ok(B)
+    assert torch.equal(out1, out2)
+    assert torch.equal(ws1, ws2)
+    v = B.workspace_views(ws2, T, d, F, E, k)
+    offs = v["offsets"].cpu().numpy()
+    row_src = v["row_src"].cpu().numpy()
+    p_got, q_got = to_np(keep[0]), to_np(keep[1])
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi == lo:
+            continue
+        xs = to_np(t["x"])[row_src[lo:hi]]
+        a, b = O.gate_up_preactivations(xs, to_np(t["W1"][e]), to_np(t["W3"][e]))
+        check_close(p_got[lo:hi], b * O.silu_grad(a), "bf16", f"{name} p[{e}]")
+        check_close(q_got[lo:hi], O.silu(a), "bf16", f"{name} q[{e}]")
