@@ -260,8 +260,9 @@ __device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_
 // p = dh/da / dh = b silu'(a) = b s (1 + a (1 - s)) and q = dh/db / dh =
 // silu(a) = a s, with s = sigmoid(a).  The backward then needs only
 // da = dh p and db = dh q.
-__device__ __forceinline__ void keep_pair(float a, float b, float& p, float& q) {
-  const float s = __frcp_rn(1.0f + __expf(-a));
+// e = exp(-a), shared with the h computation.
+__device__ __forceinline__ void keep_pair(float a, float b, float e, float& p, float& q) {
+  const float s = __frcp_rn(1.0f + e);
   q = a * s;
   p = b * (s * (1.0f + a * (1.0f - s)));
 }
@@ -517,14 +518,15 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
                 float v = s0 * __uint_as_float(a[j]);
                 if (SWIGLU) {
                   const float u = s1 * __uint_as_float(b[j]);
+                  const float ev = __expf(-v);
                   if (!W8 && args.keep != nullptr) {
                     const size_t o = (static_cast<size_t>(row0) + j) * args.ldo + col;
                     float pp, qq;
-                    keep_pair(v, u, pp, qq);
+                    keep_pair(v, u, ev, pp, qq);
                     args.keep[o] = __float2bfloat16_rn(pp);
                     args.keep[static_cast<size_t>(args.Tk) * args.ldo + o] = __float2bfloat16_rn(qq);
                   }
-                  v = v / (1.0f + __expf(-v)) * u;
+                  v = v / (1.0f + ev) * u;
                 }
                 dst[static_cast<size_t>(j) * args.ldo] = __float2bfloat16_rn(v);
               }
@@ -554,23 +556,24 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
                 u0 *= su.x;
                 u1 *= su.y;
               }
-              const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-              const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+              const float e0 = __expf(-g0), e1 = __expf(-g1);
+              const float h0 = g0 / (1.0f + e0) * u0;
+              const float h1 = g1 / (1.0f + e1) * u1;
               pk[i] = pack_bf16x2(h0, h1);
+              if (!W8 && args.keep != nullptr) {
+                // The training forward also keeps p and q (keep_pair) for the backward.
+                float p0, q0, p1, q1;
+                keep_pair(g0, u0, e0, p0, q0);
+                keep_pair(g1, u1, e1, p1, q1);
+                // In place: later iterations j > i read only g[2j], u[2j] (+1), past i.
+                g[i] = pack_bf16x2(p0, p1);
+                u[i] = pack_bf16x2(q0, q1);
+              }
             }
             uint4* dst = reinterpret_cast<uint4*>(args.out + static_cast<size_t>(grow) * args.ldo + col0 + c);
 #pragma unroll
             for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             if (!W8 && args.keep != nullptr) {
-              // The training forward also keeps p and q (keep_pair) for the backward.
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                float p0, q0, p1, q1;
-                keep_pair(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), p0, q0);
-                keep_pair(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]), p1, q1);
-                g[i] = pack_bf16x2(p0, p1);
-                u[i] = pack_bf16x2(q0, q1);
-              }
               const size_t o = static_cast<size_t>(grow) * args.ldo + col0 + c;
               uint4* dp = reinterpret_cast<uint4*>(args.keep + o);
               uint4* dq = reinterpret_cast<uint4*>(args.keep + static_cast<size_t>(args.Tk) * args.ldo + o);
