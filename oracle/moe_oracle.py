@@ -274,13 +274,15 @@ def silu_grad(a) -> np.ndarray:
     return s * (1.0 + a * (1.0 - s))
 
 
-def moe_backward(x, Wg, W1, W3, W2, k, dout, idx=None, experts=None, with_scale=False):
+def moe_backward(x, Wg, W1, W3, W2, k, dout, idx=None, experts=None, with_scale=False, weight_grads=True):
     """Gradients of L = sum(out * dout) for out = moe_forward(x, ...).
 
     ``idx`` replaces the router's choice (the weights are then the softmax
     over the chosen logits), for scoring near-tie tokens; ``experts`` limits
     the expert weight gradients to those experts (the others stay zero), to
-    bound memory at full size.  ``with_scale`` also returns, under the same
+    bound memory at full size; ``weight_grads=False`` skips dW1, dW3 and dW2
+    (returned as None), for the input gradient of a few tokens at full size
+    (a token's dx depends on that token alone).  ``with_scale`` also returns, under the same
     keys with a "_scale" suffix, each output's sum of the absolute values of
     the terms it is summed from (through the chain), the quantity rounding-
     error bounds of a computation with rounded factors are proportional to.
@@ -304,14 +306,18 @@ def moe_backward(x, Wg, W1, W3, W2, k, dout, idx=None, experts=None, with_scale=
     else:
         idx = np.asarray(idx)
         w = softmax(np.take_along_axis(router_logits(x, Wg), idx, axis=1))
-    keep = set(range(E)) if experts is None else set(experts)
+    keep = set() if not weight_grads else set(range(E)) if experts is None else set(experts)
     dx = np.zeros_like(x)
     dWg = np.zeros_like(Wg)
-    dW1, dW3, dW2 = np.zeros((E, F, d)), np.zeros((E, F, d)), np.zeros((E, d, F))
+    dW1 = dW3 = dW2 = None
+    if weight_grads:
+        dW1, dW3, dW2 = np.zeros((E, F, d)), np.zeros((E, F, d)), np.zeros((E, d, F))
     dw = np.zeros((T, k))
     if with_scale:
         sx, sWg = np.zeros_like(x), np.zeros_like(Wg)
-        s1, s3, s2 = np.zeros((E, F, d)), np.zeros((E, F, d)), np.zeros((E, d, F))
+        s1 = s3 = s2 = None
+        if weight_grads:
+            s1, s3, s2 = np.zeros((E, F, d)), np.zeros((E, F, d)), np.zeros((E, d, F))
         sdw = np.zeros((T, k))
     for j in range(k):
         for e in range(E):
@@ -354,3 +360,29 @@ def moe_backward(x, Wg, W1, W3, W2, k, dout, idx=None, experts=None, with_scale=
             np.add.at(sWg, idx[:, j], sdl[:, j][:, None] * np.abs(x))
         out.update({"dx_scale": sx, "dWg_scale": sWg, "dW1_scale": s1, "dW3_scale": s3, "dW2_scale": s2})
     return out
+
+
+def expert_grad_hidden_unit(xe, doute, we, W1e, W3e, W2e, f):
+    """The expert weight gradients that touch one hidden unit f of one
+    expert, from the rows routed to it: xe [n,d] (the tokens), doute [n,d]
+    (their output gradients) and we [n] (their gate weights for this expert).
+    The same chain rule as moe_backward, restricted to column f of h:
+      a = xe W1e[f],  b = xe W3e[f],  h = silu(a) b          (each [n])
+      dy = we dout,   dh = dy W2e[:, f]
+      da = dh b silu'(a),  db = dh silu(a)
+      dW1e[f, :] = da^T xe,  dW3e[f, :] = db^T xe,  dW2e[:, f] = dy^T h
+    Each with its sum of absolute terms ("_scale"), as moe_backward's.  A
+    hidden unit costs O(n d), so single rows and columns of the gradients can
+    be checked at full size."""
+    xe, doute = f64(xe), f64(doute)
+    we = np.asarray(we, dtype=np.float64)
+    a = xe @ f64(W1e[f])
+    b = xe @ f64(W3e[f])
+    h = silu(a) * b
+    dy = we[:, None] * doute
+    dh = dy @ f64(W2e[:, f])
+    da = dh * b * silu_grad(a)
+    db = dh * silu(a)
+    axe = np.abs(xe)
+    return {"dW1": da @ xe, "dW3": db @ xe, "dW2": dy.T @ h,
+            "dW1_scale": np.abs(da) @ axe, "dW3_scale": np.abs(db) @ axe, "dW2_scale": np.abs(dy).T @ np.abs(h)}

@@ -608,4 +608,26 @@ def pin_backward_dense_reduction_autograd(o):
     assert np.all(g["dWg"] == 0.0)
 
 
+def pin_backward_hidden_unit_slice(o):
+    """expert_grad_hidden_unit (one hidden unit's gradients, from that
+    expert's rows) equals the corresponding rows of dW1, dW3 and columns of
+    dW2 (and of their scales) of the full moe_backward."""
+    L = _tiny_layer(99, T=16, d=8, F=6, E=4)
+    k = 2
+    dout = _rng(100).standard_normal((16, 8))
+    g = o.moe_backward(L["x"], L["Wg"], L["W1"], L["W3"], L["W2"], k, dout, with_scale=True)
+    w, idx, _ = o.router(L["x"], L["Wg"], k)
+    for e in range(4):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        for f in range(6):
+            s = o.expert_grad_hidden_unit(L["x"][tok], dout[tok], w[tok, slot], L["W1"][e], L["W3"][e], L["W2"][e], f)
+            for n, got, want in (("dW1", s["dW1"], g["dW1"][e, f]), ("dW3", s["dW3"], g["dW3"][e, f]),
+                                 ("dW2", s["dW2"], g["dW2"][e, :, f])):
+                assert np.allclose(got, want, rtol=1e-12, atol=1e-13), (n, e, f)
+                assert np.allclose(s[n + "_scale"], g[n + "_scale"][e, f] if n != "dW2"
+                                   else g[n + "_scale"][e, :, f], rtol=1e-12, atol=1e-13), (n, e, f)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -163,3 +163,44 @@ def test_forward_train_keeps_swiglu_derivatives(B, name):
         a, b = O.gate_up_preactivations(xs, to_np(t["W1"][e]), to_np(t["W3"][e]))
         check_close(p_got[lo:hi], b * O.silu_grad(a), "bf16", f"{name} p[{e}]")
         check_close(q_got[lo:hi], O.silu(a), "bf16", f"{name} q[{e}]")
+
+
+def test_backward_full_size_sampled(B):
+    """The backward at T=4096 with Mixtral shapes, in the configuration
+    bench.py times (the training forward keeps p and q, then
+    moe_backward_ws), checked on outputs the oracle computes one by one:
+    dx of 12 sampled tokens (a token's dx depends on that token alone), and
+    for 2 experts x 3 hidden units the row of dW1 and of dW3 and the column of
+    dW2, over all of that expert's routed rows (expert_grad_hidden_unit)."""
+    wl = mw.get("prefill_bwd")
+    t = mw.make_inputs(wl)
+    T, d, F, E, k = wl.T, wl.d, wl.F, wl.E, wl.k
+    dout = t["dout"]
+    g = {n: v.to(DEV).contiguous() for n, v in t.items()}
+    saved = B.workspace(T, d, F, E, k)
+    _, keep = B.moe_forward_train_ws(g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved)
+    ws = torch.empty(B.moe_backward_workspace_bytes(T, d, F, E, k), dtype=torch.uint8, device=DEV)
+    grads = B.moe_backward_ws(g["dout"], g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], k, saved, ws, keep=keep)
+    status_ok(B)
+    v = B.workspace_views(saved, T, d, F, E, k)
+    gidx, gw = v["idx"].cpu().numpy(), v["w"].cpu().numpy()
+    ora_w, ora_idx, logits = O.router(t["x"], t["Wg"], k)
+    check_routing(gidx, gw, ora_idx, ora_w, logits, k)
+    w_eff, idx_eff = effective_routing(gidx, ora_w, ora_idx, logits)
+    rng = np.random.default_rng(11)
+    S = np.sort(rng.choice(T, 12, replace=False))
+    St = torch.from_numpy(S)
+    ref = O.moe_backward(t["x"][St], t["Wg"], t["W1"], t["W3"], t["W2"], k, dout[St], idx=idx_eff[S],
+                         with_scale=True, weight_grads=False)
+    check_backward_close(to_np(grads["dx"][S.tolist()]), ref["dx"], ref["dx_scale"], "full-size dx (sampled tokens)")
+    counts = np.bincount(idx_eff.ravel(), minlength=E)
+    for e in (int(np.argmax(counts)), int(np.argmin(counts))):
+        tok, slot = np.nonzero(idx_eff == e)
+        tt = torch.from_numpy(tok)
+        for f in rng.choice(F, 3, replace=False):
+            f = int(f)
+            r = O.expert_grad_hidden_unit(t["x"][tt], dout[tt], w_eff[tok, slot], t["W1"][e], t["W3"][e],
+                                          t["W2"][e], f)
+            check_backward_close(to_np(grads["dW1"][e, f]), r["dW1"], r["dW1_scale"], f"full-size dW1[{e},{f}]")
+            check_backward_close(to_np(grads["dW3"][e, f]), r["dW3"], r["dW3_scale"], f"full-size dW3[{e},{f}]")
+            check_backward_close(to_np(grads["dW2"][e, :, f]), r["dW2"], r["dW2_scale"], f"full-size dW2[{e},:,{f}]")
