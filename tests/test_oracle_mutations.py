@@ -255,6 +255,17 @@ def _bwd_transposed_dw1(m):
     m.moe_backward = bwd
 
 
+def _slice_drops_gate_weight(m):
+    src = m.expert_grad_hidden_unit
+    m.expert_grad_hidden_unit = lambda xe, doute, we, W1e, W3e, W2e, f: src(
+        xe, doute, np.ones(len(we)), W1e, W3e, W2e, f)
+
+
+def _slice_gate_up_swapped(m):
+    src = m.expert_grad_hidden_unit
+    m.expert_grad_hidden_unit = lambda xe, doute, we, W1e, W3e, W2e, f: src(xe, doute, we, W3e, W1e, W2e, f)
+
+
 MUTANTS = {f.__name__[1:]: f for f in [
     _swap_gate_up, _silu_sign, _silu_is_sigmoid, _no_renormalise, _ascending_topk,
     _ties_to_higher_index, _drop_gate_weight, _only_first_slot, _transposed_down,
@@ -262,7 +273,8 @@ MUTANTS = {f.__name__[1:]: f for f in [
     _block_no_residual, _block_unnormalised, _two_matrix_expert, _dispatch_unstable,
     _dispatch_token_not_pair, _hidden_no_gate, _rms32_no_square, _int8_divisor_128, _int8_truncates,
     _int8_ties_away_from_zero, _int8_per_column, _w8_drops_scale, _bwd_silu_grad_is_silu,
-    _bwd_silu_grad_drops_term, _bwd_no_softmax_jacobian, _bwd_drops_gate_weight, _bwd_transposed_dw1]}
+    _bwd_silu_grad_drops_term, _bwd_no_softmax_jacobian, _bwd_drops_gate_weight, _bwd_transposed_dw1,
+    _slice_drops_gate_weight, _slice_gate_up_swapped]}
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
