@@ -258,9 +258,17 @@ int moe_expert_down_w8(const void* h_perm, const int32_t* offsets, const int8_t*
 /*
  * The whole bf16 layer with int8 expert weights (a1..a6).  x[T,d], Wg[E,d],
  * out[T,d] bf16; the six weight arguments as above.  _ws takes caller scratch
- * of moe_forward_workspace_bytes(T, d, dff, E, k, MOE_DTYPE_BF16) bytes
- * (256-byte aligned); the other takes it from cudaMallocAsync on `stream`.
+ * (256-byte aligned) of at least moe_forward_workspace_bytes(T, d, dff, E, k,
+ * MOE_DTYPE_BF16) bytes; the other takes it from cudaMallocAsync on `stream`.
+ *
+ * Two forms compute the same products (codes times per-row scales, fp32
+ * accumulation).  Few rows: the GEMMs widen each weight tile from int8 on the
+ * SM.  When the experts average >= 512 routed rows (T*k >= 512*E) and the
+ * scratch holds moe_forward_w8_workspace_bytes() (3*E*dff*d*2 bytes more,
+ * the alloc form always does), the codes are widened once per call into that
+ * scratch and the bf16 GEMMs apply the scales in their epilogue.
  */
+size_t moe_forward_w8_workspace_bytes(int T, int d, int dff, int E, int k);
 int moe_forward_w8_ws(const void* x, const void* Wg, const int8_t* W1q, const float* W1s, const int8_t* W3q,
                       const float* W3s, const int8_t* W2q, const float* W2s, void* out, int T, int d, int dff,
                       int E, int k, void* workspace, size_t workspace_bytes, moe_stream_t stream);

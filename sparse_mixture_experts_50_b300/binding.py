@@ -40,6 +40,7 @@ SIGNATURES = {
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "moe_forward_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_forward_w8_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward_workspace_offsets": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "moe_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -248,6 +249,13 @@ def workspace(T, d, dff, E, k, dtype=MOE_DTYPE_BF16, device="cuda", host=False):
     """A uint8 device tensor big enough for moe_forward_ws (or moe_forward_host)."""
     fn = lib().moe_forward_host_workspace_bytes if host else lib().moe_forward_workspace_bytes
     return torch.empty(max(int(fn(T, d, dff, E, k, dtype)), 256), dtype=torch.uint8, device=device)
+
+
+def w8_workspace(T, d, dff, E, k, device="cuda"):
+    """Scratch for the int8 layer (moe_forward_w8_ws, moe_forward_ex with int8
+    weights) that lets large batches widen the codes once per call."""
+    n = int(lib().moe_forward_w8_workspace_bytes(T, d, dff, E, k))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def moe_forward_ws(x, Wg, W1, W3, W2, k, ws, out=None, stream=None):

@@ -184,7 +184,9 @@ struct GemmArgs {
   const int32_t* offsets;  // [E+1], device
   __nv_bfloat16* out;      // [Tk, ldo]
   const float* scale0;     // int8 path: row scales of B0 [E * b_rows]
-  const float* scale1;     // int8 path: row scales of B1 (gate/up only)
+  const float* scale1;     // int8 path: row scales of B1 (gate/up only); also set,
+                           // with bf16 B holding the widened int8 codes, for the
+                           // int8 layer at large batch (scaled in the epilogue)
   __nv_bfloat16* keep;     // bf16 gate/up, optional (training): the SwiGLU's
                            // local derivatives, planes [2, Tk, ldo] (see keep_pair)
   int ldo;                 // row stride of out (elements)
@@ -480,6 +482,7 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
     // -------------------------------------------------- epilogue (warps 2-5)
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. +31
     const int row_in_tile = quad * 32 + lane;
+    const bool scaled = W8 || args.scale0 != nullptr;  // per-weight-row scales in the epilogue
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -509,8 +512,8 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
           const int col = SWIGLU ? n * BN_HALF + row_in_tile : n * BN + hf * BN_HALF + row_in_tile;
           if (col < args.n_out) {
             const size_t srow = static_cast<size_t>(e) * args.b_rows + col;
-            const float s0 = W8 ? __ldg(args.scale0 + srow) : 1.0f;
-            const float s1 = (W8 && SWIGLU) ? __ldg(args.scale1 + srow) : 1.0f;
+            const float s0 = scaled ? __ldg(args.scale0 + srow) : 1.0f;
+            const float s1 = (scaled && SWIGLU) ? __ldg(args.scale1 + srow) : 1.0f;
             __nv_bfloat16* dst = args.out + static_cast<size_t>(row0) * args.ldo + col;
 #pragma unroll
             for (int j = 0; j < TN; ++j) {
@@ -548,7 +551,7 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
             for (int i = 0; i < 16; ++i) {
               float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
               float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-              if (W8) {
+              if (scaled) {
                 const float2 sg = __ldg(reinterpret_cast<const float2*>(args.scale0 + srow) + i);
                 const float2 su = __ldg(reinterpret_cast<const float2*>(args.scale1 + srow) + i);
                 g0 *= sg.x;
@@ -598,7 +601,7 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               float y0 = __uint_as_float(v[2 * i]), y1 = __uint_as_float(v[2 * i + 1]);
-              if (W8) {
+              if (scaled) {
                 const float2 sy = __ldg(reinterpret_cast<const float2*>(args.scale0 + srow) + i);
                 y0 *= sy.x;
                 y1 *= sy.y;
@@ -921,6 +924,17 @@ int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1
 int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d, int dff, int E,
                    const Ctx& c, cudaStream_t s) {
   return launch_gemm<false, false>(h, W2, nullptr, nullptr, nullptr, offsets, y, Tk, dff, d, d, E, c, s);
+}
+
+int launch_tc_gate_up_scaled(const void* x_perm, const int32_t* offsets, const void* W1c, const float* W1s,
+                             const void* W3c, const float* W3s, void* h, int Tk, int d, int dff, int E, const Ctx& c,
+                             cudaStream_t s) {
+  return launch_gemm<true, false>(x_perm, W1c, W3c, W1s, W3s, offsets, h, Tk, d, dff, dff, E, c, s);
+}
+
+int launch_tc_down_scaled(const void* h, const int32_t* offsets, const void* W2c, const float* W2s, void* y, int Tk,
+                          int d, int dff, int E, const Ctx& c, cudaStream_t s) {
+  return launch_gemm<false, false>(h, W2c, nullptr, W2s, nullptr, offsets, y, Tk, dff, d, d, E, c, s);
 }
 
 int launch_w8_gate_up(const void* x_perm, const int32_t* offsets, const int8_t* W1q, const float* W1s,

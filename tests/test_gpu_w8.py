@@ -148,6 +148,34 @@ def test_forward_w8_small(B, name, entry):
     check_close(to_np(out), ref, "bf16", f"{name} int8-weight layer")
 
 
+@pytest.mark.parametrize("scratch", ["narrow", "wide"])
+def test_forward_w8_both_forms(B, scratch):
+    """T*k >= 512*E: with moe_forward_w8_workspace_bytes of scratch the layer
+    widens the codes once and runs the bf16 GEMMs with epilogue scales; with
+    the plain layer scratch it widens tiles inside the GEMMs.  Both against
+    the oracle's layer of the dequantised weights, with ragged experts."""
+    wl = mw.Workload("w8_wide", 1100, 320, 448, 2, 1, "bf16", "std002")
+    assert wl.T * wl.k >= 512 * wl.E
+    t = mw.make_inputs(wl)
+    qs = [O.quantize_int8_rows(t[n]) for n in ("W1", "W3", "W2")]
+    args = [dev(torch.from_numpy(v)) for qv in qs for v in qv]
+    x, Wg = dev(t["x"]), dev(t["Wg"])
+    if scratch == "wide":
+        ws = B.w8_workspace(wl.T, wl.d, wl.F, wl.E, wl.k)
+        assert ws.numel() > B.workspace(wl.T, wl.d, wl.F, wl.E, wl.k).numel()
+    else:
+        ws = B.workspace(wl.T, wl.d, wl.F, wl.E, wl.k)
+    out = B.moe_forward_w8_ws(x, Wg, *args, wl.k, ws)
+    status_ok(B)
+    ref, ora_w, ora_idx, logits = O.moe_forward_w8(t["x"], t["Wg"], *(v for qv in qs for v in qv), wl.k)
+    idx, _ = B.moe_router_topk(x, Wg, wl.k)
+    w_eff, idx_eff = effective_routing(to_np(idx), ora_w, ora_idx, logits)
+    if not np.array_equal(idx_eff, ora_idx):
+        D = [O.dequantize_int8_rows(*qv) for qv in qs]
+        ref = O.moe_forward_with_routing(t["x"], *D, w_eff, idx_eff)
+    check_close(to_np(out), ref, "bf16", f"int8 layer, {scratch} scratch")
+
+
 def test_forward_w8_matches_bf16_layer_within_quantisation(B):
     """The int8 layer is the same layer: its output stays within the
     quantisation error of the bf16 layer's (the oracle pins the same bound)."""
