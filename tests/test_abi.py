@@ -110,3 +110,40 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         B.moe_router_topk(x, torch.zeros(8, 64, dtype=torch.bfloat16), 2)
+
+
+def test_w8_workspace_bytes(lib):
+    """The int8 layer asks for the codes' widened copy (3*E*dff*d*2 bytes,
+    each matrix 256-byte aligned) exactly when the experts average at least
+    512 routed rows."""
+    d, F, E, k = 4096, 14336, 8, 2
+    base = lambda T: lib.moe_forward_workspace_bytes(T, d, F, E, k, B.MOE_DTYPE_BF16)
+    wide = 3 * ((E * F * d * 2 + 255) // 256 * 256)
+    assert lib.moe_forward_w8_workspace_bytes(16, d, F, E, k) == base(16)
+    assert lib.moe_forward_w8_workspace_bytes(4096, d, F, E, k) == base(4096) + wide
+    t0 = 512 * E // k                      # T*k == 512*E: the first T that widens
+    assert lib.moe_forward_w8_workspace_bytes(t0, d, F, E, k) == base(t0) + wide
+    assert lib.moe_forward_w8_workspace_bytes(t0 - 1, d, F, E, k) == base(t0 - 1)
+    assert lib.moe_forward_w8_workspace_bytes(-1, d, F, E, k) == 0
+
+
+def test_training_entry_validation(lib):
+    """moe_forward_train_ws needs its keep buffer; moe_backward_ws checks
+    keep's alignment and both scratch sizes before any device work."""
+    T, d, F, E, k = 16, 4096, 14336, 8, 2
+    fwd = lib.moe_forward_train_ws
+    assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, T, d, F, E, k, FAKE, 1 << 30, NULL) == B.MOE_EINVAL
+    assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 8, T, d, F, E, k, FAKE, 1 << 30, NULL) == B.MOE_EINVAL
+    assert fwd(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, d, F, E, k, NULL, 0, NULL) == B.MOE_OK
+    bwd = lib.moe_backward_ws
+    saved = lib.moe_forward_workspace_bytes(T, d, F, E, k, B.MOE_DTYPE_BF16)
+    need = lib.moe_backward_workspace_bytes(T, d, F, E, k)
+    assert need > 0
+
+    def call(keep=NULL, saved_bytes=saved, ws_bytes=need, T=T):
+        return bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, saved_bytes, keep, FAKE, FAKE, FAKE, FAKE, FAKE,
+                   T, d, F, E, k, FAKE, ws_bytes, NULL)
+    assert call(keep=FAKE + 8) == B.MOE_EINVAL          # keep not 16-byte aligned
+    assert call(saved_bytes=saved - 1) == B.MOE_ENOMEM  # saved scratch too small
+    assert call(ws_bytes=need - 1) == B.MOE_ENOMEM      # backward scratch too small
+    assert call(T=0) == B.MOE_OK
