@@ -210,10 +210,11 @@ class Layer:
 
 
 class BwdLayer:
-    """The backward of one workload: the training forward (moe_forward_train_ws,
-    which keeps the SwiGLU's local derivatives p and q) runs once at set-up with caller scratch (`saved`),
-    then step() runs moe_backward_ws through the C ABI into preallocated
-    gradients; forward_step() re-runs that training forward."""
+    """The backward of one workload.  The training forward
+    (moe_forward_train_ws, which keeps the SwiGLU's local derivatives p and
+    q) runs once at set-up with caller scratch (`saved`); step() runs
+    moe_backward_ws through the C ABI into preallocated gradients;
+    forward_step() re-runs that training forward."""
 
     def __init__(self, wl, tensors, device):
         from sparse_mixture_experts_50_b300 import binding as B
@@ -285,7 +286,8 @@ def time_layer(layer, steps, warmup, flush, dist_on):
 def bench_backward(name, shared, args, device, peaks, dist_on):
     """The backward leg: T / (mean backward time); its tensor roofline uses
     the algorithmic 12*d*F FLOP per routed row (dh 2, dx 4, dW2 2, dW1+dW3 4;
-    the recomputation of a and b is implementation work and not counted)."""
+    the forward's p and q, or a recomputation of a and b, are implementation
+    work and not counted)."""
     wl = mw.get(name)
     layer = BwdLayer(wl, make_tensors(wl, shared), device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
