@@ -608,6 +608,48 @@ def pin_backward_dense_reduction_autograd(o):
     assert np.all(g["dWg"] == 0.0)
 
 
+def pin_backward_symbolic(o):
+    """Every gradient against exact symbolic differentiation (sympy) of the
+    layer written out from the pages' definition on a hand-sized case: 2
+    tokens, d=2, F=2, E=3, k=2, small rational inputs, the routing (clear
+    logit gaps) held fixed, L = sum(out * dout).  Shares no step with the
+    oracle's chain rule."""
+    import sympy as sp
+    T, d, F, E, k = 2, 2, 2, 3, 2
+    vals = {
+        "x": [[1, -2], [sp.Rational(1, 2), 3]],
+        "Wg": [[1, 0], [0, 1], [-1, sp.Rational(1, 4)]],
+        "W1": [[[1, -1], [sp.Rational(1, 2), 2]], [[-1, 1], [2, sp.Rational(-1, 3)]], [[0, 1], [1, 1]]],
+        "W3": [[[2, 1], [-1, sp.Rational(1, 4)]], [[1, 1], [sp.Rational(1, 2), -2]], [[-1, 0], [1, -1]]],
+        "W2": [[[1, 2], [-1, sp.Rational(1, 2)]], [[sp.Rational(-1, 2), 1], [1, 1]], [[2, -1], [0, 1]]],
+    }
+    dout = [[1, sp.Rational(-1, 2)], [2, 1]]
+    sym = {n: np.array(sp.symbols(f"{n}_0:{np.array(v, dtype=object).size}"), dtype=object).reshape(
+        np.array(v, dtype=object).shape) for n, v in vals.items()}
+    subs = {sym[n].flat[i]: np.array(v, dtype=object).flat[i] for n, v in vals.items()
+            for i in range(np.array(v, dtype=object).size)}
+    silu = lambda a: a / (1 + sp.exp(-a))
+    L = 0
+    for t in range(T):
+        logit = [sum(sym["Wg"][e, c] * sym["x"][t, c] for c in range(d)) for e in range(E)]
+        num = [float(lv.xreplace(subs)) for lv in logit]
+        top = sorted(range(E), key=lambda e: -num[e])[:k]
+        assert num[top[-1]] - max(num[e] for e in range(E) if e not in top) > 0.1
+        z = [sp.exp(logit[e]) for e in top]
+        for j, e in enumerate(top):
+            w = z[j] / sum(z)
+            h = [silu(sum(sym["W1"][e, f, c] * sym["x"][t, c] for c in range(d)))
+                 * sum(sym["W3"][e, f, c] * sym["x"][t, c] for c in range(d)) for f in range(F)]
+            for c in range(d):
+                L += dout[t][c] * w * sum(sym["W2"][e, c, f] * h[f] for f in range(F))
+    num = {n: np.array(np.array(v, dtype=object), dtype=np.float64) for n, v in vals.items()}
+    g = o.moe_backward(num["x"], num["Wg"], num["W1"], num["W3"], num["W2"], k,
+                       np.array(np.array(dout, dtype=object), dtype=np.float64))
+    for n in vals:
+        want = np.array([float(sp.diff(L, s_).xreplace(subs).evalf(30)) for s_ in sym[n].flat]).reshape(num[n].shape)
+        assert np.allclose(g["d" + n], want, rtol=1e-12, atol=1e-13), n
+
+
 def pin_backward_hidden_unit_slice(o):
     """expert_grad_hidden_unit (one hidden unit's gradients, from that
     expert's rows) equals the corresponding rows of dW1, dW3 and columns of

@@ -287,4 +287,5 @@ def test_planted_mistake_is_caught(name):
             pin(m)
         except Exception:  # an assertion or a shape error both count
             caught.append(pin.__name__)
+            break  # one failing pin is enough
     assert caught, f"no pin caught the planted mistake {name!r}"
