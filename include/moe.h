@@ -194,9 +194,11 @@ int moe_block_forward(const void* x, const void* gamma, float eps, const void* W
  *    W1, W3, W2 are then ignored; bf16 only);
  *  - events (NULL, or 5 cudaEvent_t; NULL entries skipped) are recorded on
  *    `stream` before the router, after dispatch, after the gate/up GEMM,
- *    after the down GEMM and after the combine.
- * workspace as moe_forward_ws.  Same results as the corresponding entry
- * point.
+ *    after the down GEMM and after the combine (with int8 weights in the
+ *    widened-once form, the widening falls between the second and third).
+ * workspace as moe_forward_ws; with int8 weights, as moe_forward_w8_ws (the
+ * large-batch form needs moe_forward_w8_workspace_bytes()).  Same results as
+ * the corresponding entry point.
  */
 int moe_forward_ex(const void* x, const void* gamma_opt, float eps, const void* Wg, const void* W1,
                    const void* W3, const void* W2, const int8_t* W1q, const float* W1s, const int8_t* W3q,
