@@ -14,8 +14,8 @@
 //
 // One persistent tcgen05 kernel template, one CTA per SM, warp-specialised
 // like the forward kernel (warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5
-// epilogue), every operand K-major and staged by TMA with the 128-byte
-// swizzle.  The token rows are K-major; everything else is read in place
+// epilogue), every operand staged by TMA with the 128-byte swizzle.  The
+// token rows of DH, DSW and DX are K-major; everything else is read in place
 // MN-major, as TMA boxes of 64 M or N columns x 64 K rows described to
 // tcgen05 with the transpose bits: the weights of DH and DX (W2 [E,d,F] for
 // dh, W1 and W3 [E,F,d] for dx_perm, whose contiguous dimension is the
@@ -38,8 +38,8 @@
 //            W1, then db with W3) into one accumulator; two accumulators
 //            alternate between tiles.
 //   WGRAD    per expert an [M, N] fp32 matrix, tile 128 x 256, K = the
-//            expert's padded token segment; an expert with no tokens gets
-//            zeros (its tiles skip the MMAs).
+//            expert's routed rows; an expert with no tokens gets zeros (its
+//            tiles skip the MMAs).
 // Epilogue stores go through a per-warp 32 x 32 staging block in shared
 // memory, so that each store instruction writes contiguous row segments
 // (a lane per row would make every instruction touch 32 rows).
