@@ -1,0 +1,56 @@
+"""bench.py's host-side arithmetic (CPU only): the algorithmic work it
+divides by is the closed form of the layer at Mixtral shape (d=4096,
+F=14336, E=8, k=2), and the committed ncu traffic is used only on the
+kernel source it was taken on."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import moe_workloads as mw  # noqa: E402
+
+D, F, E, K = 4096, 14336, 8, 2
+
+
+def test_flops_per_token_closed_form():
+    # k experts x (3 matrices x 2 d F) + the gate's 2 d E
+    wl = mw.get("prefill")
+    flops, _, gu_flops, _ = bench.algorithmic(wl, [1] * E)
+    assert flops == wl.T * 704_708_608
+    assert gu_flops == wl.T * K * 4 * D * F == 1_924_145_348_608
+
+
+def test_decode_bytes_closed_form():
+    wl = mw.get("decode")
+    _, nbytes, _, gu_bytes = bench.algorithmic(wl, [4] * E)
+    per_expert = 3 * D * F * 2
+    assert per_expert == 352_321_536
+    assert nbytes == 8 * per_expert + D * E * 2 + 2 * wl.T * D * 2
+    assert gu_bytes == 8 * 2 * D * F * 2 == 1_879_048_192
+
+
+def test_unused_experts_are_not_counted():
+    wl = mw.get("skewed_zero")
+    _, n8, _, g8 = bench.algorithmic(wl, [1] * E)
+    _, n7, _, g7 = bench.algorithmic(wl, [1] * (E - 1) + [0])
+    assert n8 - n7 == 3 * D * F * 2
+    assert g8 - g7 == 2 * D * F * 2
+
+
+def test_int8_bytes_are_codes_plus_scales():
+    wl = mw.get("decode_w8")
+    _, nbytes, _, gu_bytes = bench.algorithmic(wl, [4] * E)
+    assert gu_bytes == 8 * (2 * D * F + 2 * F * 4)
+    assert nbytes == 8 * (3 * D * F + (2 * F + D) * 4) + D * E * 2 + 2 * wl.T * D * 2
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "decode_w8"])
+def test_ncu_traffic_only_on_matching_source(name, tmp_path, monkeypatch):
+    got = bench.ncu_traffic(name)
+    assert got is None or got > 0
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0000000000000000")
+    assert bench.ncu_traffic(name) is None
