@@ -167,32 +167,6 @@ __device__ __forceinline__ void warp_transpose_f32(uint32_t* stg, const float (&
   __syncwarp();
 }
 
-// Rows r < rows of a bf16 src (row stride ld, 32 columns each): t[i] holds
-// row 2i + lane/16, columns 2(lane%16), +1 (two 64-byte rows per
-// instruction); rows past `rows` read as zero.
-__device__ __forceinline__ void warp_load_rows_bf16(const __nv_bfloat16* src, size_t ld, int rows, int lane,
-                                                    uint32_t (&t)[16]) {
-  const int half = lane >> 4, w = lane & 15;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int r = 2 * i + half;
-    t[i] = r < rows ? __ldg(reinterpret_cast<const unsigned int*>(src + r * ld) + w) : 0u;
-  }
-}
-
-// The transpose of what warp_load_rows_bf16 read: lane = row, pk[i] =
-// columns 2i, 2i+1.
-__device__ __forceinline__ void warp_transpose_bf16(uint32_t* stg, const uint32_t (&t)[16], int lane,
-                                                    uint32_t (&pk)[16]) {
-  const int half = lane >> 4, w = lane & 15;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) stg[(2 * i + half) * 17 + w] = t[i];
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < 16; ++i) pk[i] = stg[lane * 17 + i];
-  __syncwarp();
-}
-
 // The SwiGLU derivative for h = silu(a) b, given dh = g:
 // da = g b silu'(a) with silu'(a) = s (1 + a (1 - s)), s = sigmoid(a); db = g silu(a).
 __device__ __forceinline__ void swiglu_grad(float g, float a, float b, float& da, float& db) {
