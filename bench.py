@@ -18,6 +18,12 @@ Per-kernel events inside the step give the dominant kernel's roofline.
 "e2e" runs moe_forward_host with pinned host activations (host->device copy,
 the layer, device->host copy, synchronise) timed by the host clock.
 
+Accuracy (part of the CPU-baseline leg, after the timed steps, skipped with
+--no-cpu-baseline): every forward workload's routing and a sample of its
+outputs are scored by the fp64 CPU oracle - near-tie tokens, those routed
+differently, clear tokens routed differently (0), rel-L2 - and the line's
+"targets" states the layer roofline fractions against the ones required.
+
 Multi-GPU (torchrun): replicas only - every rank runs the same workload on its
 own GPU with no collective on the data path; value = tokens of all ranks /
 max over ranks of the timed region.  ``--impl reference`` times the fp64 CPU
@@ -316,11 +322,10 @@ def bench_backward(name, shared, args, device, peaks, dist_on):
     fwd = sum(a.elapsed_time(b) for a, b in fwd_ms) / len(fwd_ms)
     return {
         "workload": name, "T": wl.T, "tokens_per_s": wl.T / (ms * 1e-3), "ms_per_step": ms,
-        "train_forward_ms": fwd,
+        "ms_per_step_median": statistics.median(step_ms), "train_forward_ms": fwd,
         "layer_roofline_frac": achieved / peaks["bf16_tflops"], "bound": "tensor",
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],
-                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "kernel": "whole backward (moe_backward_ws)", "algorithmic_per_launch": flops, "traffic": None},
         "wall_s": wall,
     }, layer
@@ -352,12 +357,12 @@ def bench_workload(name, shared, args, device, peaks, dist_on):
         achieved, peak, unit = gu_flops / (gu_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     res = {
         "workload": name, "T": wl.T, "tokens_per_s": wl.T / (ms * 1e-3), "ms_per_step": ms,
+        "ms_per_step_median": statistics.median(step_ms),
         "layer_roofline_frac": t_roof / (ms * 1e-3), "bound": bound,
         "layer_roofline_tokens_per_s": wl.T / t_roof,
         "kernel_ms": {p: sum(v) / len(v) for p, v in parts.items()},
         "expert_counts": counts,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     **({"frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]} if bound == "tensor" else {}),
                      "kernel": "grouped_gemm_tc_kernel<gate_up+SwiGLU%s>" % (", int8 weights" if wl.w8 else ""),
                      "algorithmic_per_launch": gu_bytes if bound == "hbm" else gu_flops,
                      "traffic": ncu_traffic(name)},
@@ -415,6 +420,104 @@ def cpu_baseline(name, tensors, reps=3):
     return {"value": n / el, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": f"{name}: tokens 0-{n - 1} of {wl.T}, whole layer in fp64 (numpy), median of {reps} runs, "
                       f"{el:.2f} s each"}
+
+
+NEAR_TIE = 1e-3          # oracle logit gap below which a token's routing may legitimately differ
+ACCURACY_SAMPLE = 64     # seeded tokens per workload whose outputs the oracle scores
+# Layer roofline fractions the layer must reach (bound, target).
+TARGETS = {"decode": ("hbm", 0.70), "skewed": ("tensor", 0.60), "skewed_zero": ("tensor", 0.60),
+           "block": ("tensor", 0.60)}
+_CODES = {}              # the oracle's int8 codes of an expert matrix, by (tensor id, expert)
+
+
+class _OracleInt8Experts:
+    """An [E, rows, cols] expert tensor as the int8 layer uses it: each
+    expert quantised by the oracle and dequantised when indexed (one expert
+    at a time; the codes are cached, the fp64 values are not)."""
+
+    def __init__(self, W):
+        self.W = W
+        self.shape = tuple(W.shape)
+
+    def __getitem__(self, e):
+        import oracle.moe_oracle as O
+        key = (id(self.W), int(e))
+        if key not in _CODES:
+            _CODES[key] = O.quantize_int8_rows(self.W[e])
+        return O.dequantize_int8_rows(*_CODES[key])
+
+
+def accuracy(layer, tensors, sample=ACCURACY_SAMPLE):
+    """The GPU result of one workload scored by the fp64 oracle, after the
+    timed steps (part of the CPU-baseline leg; nothing here is timed).
+
+    Routing, on every token: the oracle's fp64 logits decide which tokens are
+    near ties (a gap below 1e-3 among the k+1 largest logits; in the block
+    form widened by the logit change of the rare normalised element the two
+    sides round apart); counted are those tokens, those of them the GPU routed
+    differently, and clear tokens the GPU routed differently (must be 0).
+    Output: rel-L2 of the layer output over a seeded sample of tokens plus
+    every near-tie token, against the oracle run on the GPU's routing where a
+    near tie went the other way (block form: also of the MoE delta alone)."""
+    import numpy as np
+
+    import oracle.moe_oracle as O
+    wl = layer.wl
+    t0 = time.perf_counter()
+    if wl.block:
+        xin = O.block_normed_input(tensors["x"], tensors["gamma"], wl.eps)
+        dl = (layer.xn.cpu().double().numpy() - xin) @ O.f64(tensors["Wg"]).T
+        extra = np.max(np.abs(dl), axis=1)
+    else:
+        xin = O.f64(tensors["x"])
+        extra = np.zeros(wl.T)
+    ora_w, ora_idx, logits = O.router(xin, tensors["Wg"], wl.k)
+    gi = layer.idx.cpu().numpy().astype(np.int64)
+    top = -np.sort(-logits, axis=1)[:, : wl.k + 1]
+    near = np.any(top[:, :-1] - top[:, 1:] < (NEAR_TIE + 2.0 * extra)[:, None], axis=1)
+    differ = np.any(gi != ora_idx, axis=1)
+    rng = np.random.default_rng(1)
+    toks = set(rng.choice(wl.T, size=min(sample, wl.T), replace=False).tolist()) | set(np.nonzero(near)[0].tolist())
+    s = np.array(sorted(toks))
+    w_eff, idx_eff = ora_w[s].copy(), ora_idx[s].copy()
+    for i, t in enumerate(s):
+        if near[t] and differ[t]:
+            idx_eff[i] = gi[t]
+            w_eff[i] = O.softmax(logits[t, gi[t]])
+    if wl.w8:
+        W1, W3, W2 = (_OracleInt8Experts(tensors[n]) for n in ("W1", "W3", "W2"))
+    else:
+        W1, W3, W2 = tensors["W1"], tensors["W3"], tensors["W2"]
+    t1 = time.perf_counter()
+    delta = O.moe_forward_with_routing(xin[s], W1, W3, W2, w_eff, idx_eff)
+    oracle_s = time.perf_counter() - t1
+
+    def rel(got, ref):
+        return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+    out = layer.out.cpu().double().numpy()[s]
+    res = {"near_tie_tokens": int(near.sum()), "near_tie_routed_differently": int((near & differ).sum()),
+           "clear_tokens_routed_differently": int((~near & differ).sum()),
+           "rel_l2": rel(out, delta + (O.f64(tensors["x"][s]) if wl.block else 0.0)),
+           "rel_l2_bound": 5e-3, "scored_tokens": int(s.size)}
+    if wl.block:
+        gd = layer.B.moe_combine(layer.y, layer.slot_pos, layer.w, wl.T)
+        res["rel_l2_moe_delta"] = rel(gd.cpu().double().numpy()[s], delta)
+    res["oracle_tokens_per_s"] = s.size / oracle_s
+    res["wall_s"] = time.perf_counter() - t0
+    return res
+
+
+def targets_of(results):
+    """The layer roofline fractions the layer is held to, from this run."""
+    out = {}
+    for name, (bound, target) in TARGETS.items():
+        r = results.get(name)
+        if r is None:
+            continue
+        out[name] = {"bound": bound, "layer_frac": round(r["layer_roofline_frac"], 4), "target": target,
+                     "met": bool(r["bound"] == bound and r["layer_roofline_frac"] >= target)}
+    return out
 
 
 def job_throughput(tokens_local, t_local, dist_on, device):
@@ -520,6 +623,8 @@ def main():
         clocks.start()
         res, layer = bench_workload(name, shared, args, device, peaks, dist_on)
         res["clocks"] = clocks.stop()
+        if rank == 0 and not args.no_cpu_baseline and not mw.get(name).bwd:
+            res["accuracy"] = accuracy(layer, make_tensors(mw.get(name), shared))
         if name == head_name:
             head_layer = layer
         else:
@@ -553,6 +658,10 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": KERNELS_PER_STEP[mw.get(head_name).block] * args.steps,
             "clocks": head.get("clocks"),
+            "targets": targets_of(results),
+            "accuracy": {n: {k: r["accuracy"][k] for k in ("near_tie_tokens", "near_tie_routed_differently",
+                                                           "clear_tokens_routed_differently", "rel_l2")}
+                         for n, r in results.items() if "accuracy" in r},
             "workloads": {n: {**{k: v for k, v in r.items() if k != "clocks"},
                               "sm_mhz": (r.get("clocks") or {}).get("sm_mhz")} for n, r in results.items()},
         }

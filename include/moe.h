@@ -124,10 +124,25 @@ int moe_expert_gate_up(const void* x_perm, const int32_t* offsets, const void* W
 int moe_expert_down(const void* h_perm, const int32_t* offsets, const void* W2,
                     void* y_perm, int Tk, int d, int dff, int E, int dtype, moe_stream_t stream);
 
-/* Steps a4 + a5 in one call; h_perm[Tk,dff] is caller-provided scratch. */
+/*
+ * Steps a4 + a5 in one call (section 04: each expert's whole SwiGLU):
+ *   y_perm[p] = W2_e (silu(W1_e x_perm[p]) * (W3_e x_perm[p]))  for p in expert e's rows.
+ * x_perm[Tk,d] in, y_perm[Tk,d] out (dtype), offsets[E+1] in (device).  The
+ * hidden activations h[Tk,dff] live in scratch taken from cudaMallocAsync
+ * on `stream` (the device's stream-ordered pool) and released on the same
+ * stream; MOE_ENOMEM if that allocation fails.
+ */
 int moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3,
-                   const void* W2, void* h_perm, void* y_perm, int Tk, int d, int dff, int E,
-                   int dtype, moe_stream_t stream);
+                   const void* W2, void* y_perm, int Tk, int d, int dff, int E, int dtype,
+                   moe_stream_t stream);
+
+/*
+ * As moe_expert_ffn on caller scratch: h_perm[Tk,dff] (dtype, 16-byte
+ * aligned) receives the hidden activations silu(W1_e x) * (W3_e x).
+ */
+int moe_expert_ffn_ws(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3,
+                      const void* W2, void* h_perm, void* y_perm, int Tk, int d, int dff, int E,
+                      int dtype, moe_stream_t stream);
 
 /*
  * Step a6 - combine fused with the un-permute (section 05, class MoE adds the
@@ -139,8 +154,11 @@ int moe_combine(const void* y_perm, const int32_t* slot_pos, const float* topk_w
                 const void* residual_opt, void* out, int T, int d, int k, int dtype,
                 moe_stream_t stream);
 
-/* Bytes of scratch moe_forward_ws / moe_block_forward_ws need. */
-size_t moe_forward_workspace_bytes(int T, int d, int dff, int E, int k, int dtype);
+/*
+ * Bytes of scratch moe_forward_ws, moe_block_forward_ws and moe_forward_ex
+ * (bf16 or fp32 experts) need for T tokens; 0 for invalid sizes.
+ */
+size_t moe_workspace_bytes(int T, int d, int dff, int E, int k, int dtype);
 
 /*
  * Byte offsets of the layer's intermediates inside that scratch (host
@@ -154,7 +172,7 @@ int moe_forward_workspace_offsets(int T, int d, int dff, int E, int k, int dtype
 
 /*
  * The whole layer, a1..a6, on caller-provided scratch `workspace` of at least
- * moe_forward_workspace_bytes() bytes (256-byte aligned).  dtype selects the
+ * moe_workspace_bytes() bytes (256-byte aligned).  dtype selects the
  * bf16 tensor-core path or the fp32 path.
  */
 int moe_forward_ws(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2,
@@ -210,7 +228,7 @@ int moe_forward_ex(const void* x, const void* gamma_opt, float eps, const void* 
  * End-to-end call with HOST activations: copies x_host[T,d] (pinned host
  * memory for best speed) to the device, runs moe_forward_ws, and copies the
  * result back to out_host[T,d].  Weights stay resident on the device.
- * `workspace` must hold moe_forward_workspace_bytes() + 2*T*d*elem bytes.
+ * `workspace` must hold moe_workspace_bytes() + 2*T*d*elem bytes.
  * Synchronises `stream` before returning, so out_host is ready on return.
  */
 size_t moe_forward_host_workspace_bytes(int T, int d, int dff, int E, int k, int dtype);
@@ -260,7 +278,7 @@ int moe_expert_down_w8(const void* h_perm, const int32_t* offsets, const int8_t*
 /*
  * The whole bf16 layer with int8 expert weights (a1..a6).  x[T,d], Wg[E,d],
  * out[T,d] bf16; the six weight arguments as above.  _ws takes caller scratch
- * (256-byte aligned) of at least moe_forward_workspace_bytes(T, d, dff, E, k,
+ * (256-byte aligned) of at least moe_workspace_bytes(T, d, dff, E, k,
  * MOE_DTYPE_BF16) bytes; the other takes it from cudaMallocAsync on `stream`.
  *
  * Two forms compute the same products (codes times per-row scales, fp32
@@ -345,7 +363,7 @@ int moe_backward(const void* dout, const void* x, const void* Wg, const void* W1
  *    the process exits.  Nothing is allocated per call (no cudaMalloc,
  *    cudaMallocAsync or cudaFree).
  *  - A layer that needs more scratch than that, i.e.
- *    moe_forward_workspace_bytes(T, d, dff, E, k, MOE_DTYPE_BF16) >
+ *    moe_workspace_bytes(T, d, dff, E, k, MOE_DTYPE_BF16) >
  *    MOE_NOALLOC_SCRATCH_BYTES (at d=4096, d_ff=14336, k=2: T > 170), is
  *    rejected with MOE_ENOMEM before anything is enqueued.
  *  - The first call on a device looks up the array's device address with

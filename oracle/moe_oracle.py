@@ -157,6 +157,56 @@ def dispatch(idx, E):
     return counts, offsets, row_src, slot_pos
 
 
+# ---------------------------------------------------------------- grouped steps
+# The layer's steps on rows already grouped by expert (the order `dispatch`
+# gives): rows offsets[e] .. offsets[e+1]-1 belong to expert e.  Section 05's
+# MoE loop applies each expert to the tokens routed to it; these functions
+# apply the same per-expert maps to those rows, one expert at a time.
+def gate_up_projection(x_perm, offsets, W1, W3) -> np.ndarray:
+    """Section 04, SwiGLUFeedForward, first half, per expert segment:
+    h[p] = silu(W1_e x_perm[p]) * (W3_e x_perm[p]) for the rows p of expert e.
+    Returns h[Tk,F]."""
+    x_perm = f64(x_perm)
+    offsets = np.asarray(offsets)
+    out = np.zeros((x_perm.shape[0], W1.shape[1]))
+    for e in range(W1.shape[0]):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            out[a:b] = swiglu_hidden(x_perm[a:b], W1[e], W3[e])
+    return out
+
+
+def down_projection(h, offsets, W2) -> np.ndarray:
+    """Section 04, SwiGLUFeedForward, the down projection, per expert
+    segment: y[p] = W2_e h[p] for the rows p of expert e.  h[Tk,F],
+    W2[E,d,F]; returns y[Tk,d]."""
+    h = f64(h)
+    offsets = np.asarray(offsets)
+    out = np.zeros((h.shape[0], W2.shape[1]))
+    for e in range(W2.shape[0]):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            out[a:b] = h[a:b] @ f64(W2[e]).T
+    return out
+
+
+def combine(y_perm, slot_pos, w, residual=None) -> np.ndarray:
+    """Section 05, class MoE: each token's output is the sum over its k
+    slots of the slot's gate weight times the output of the slot's expert;
+    section 06 (Block) adds the residual.  The output of pair (t, j) is row
+    slot_pos[t*k + j] of y_perm.  Returns out[T,d]."""
+    y = f64(y_perm)
+    w = np.asarray(w, dtype=np.float64)
+    T, k = w.shape
+    pos = np.asarray(slot_pos).reshape(T, k)
+    out = np.zeros((T, y.shape[1]))
+    for j in range(k):
+        out += w[:, j][:, None] * y[pos[:, j]]
+    if residual is not None:
+        out += f64(residual)
+    return out
+
+
 # ---------------------------------------------------------------- layer
 def moe_forward_with_routing(x, W1, W3, W2, w, idx) -> np.ndarray:
     """Section 05, MoE.forward given the router's (w, idx).

@@ -13,11 +13,12 @@ from .binding import (  # noqa: F401
     moe_combine,
     moe_expert_down,
     moe_expert_ffn,
+    moe_expert_ffn_ws,
     moe_expert_gate_up,
     moe_forward,
     moe_forward_f32,
     moe_forward_host,
-    moe_forward_workspace_bytes,
+    moe_workspace_bytes,
     moe_forward_ws,
     moe_get_device_status,
     moe_permute,

@@ -37,9 +37,10 @@ SIGNATURES = {
     "moe_permute": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P]),
     "moe_expert_gate_up": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_expert_down": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
-    "moe_expert_ffn": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "moe_expert_ffn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "moe_expert_ffn_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
-    "moe_forward_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_w8_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_forward_workspace_offsets": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "moe_forward_ws": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
@@ -194,8 +195,20 @@ def moe_expert_down(h_perm, offsets, W2, y_perm=None, stream=None):
     return y_perm
 
 
-def moe_expert_ffn(x_perm, offsets, W1, W3, W2, h_perm=None, y_perm=None, stream=None):
-    """Steps a4 + a5: returns y_perm[Tk,d]."""
+def moe_expert_ffn(x_perm, offsets, W1, W3, W2, y_perm=None, stream=None):
+    """Steps a4 + a5 (hidden activations in pool scratch): returns y_perm[Tk,d]."""
+    _dev(x_perm, offsets, W1, W3, W2, y_perm)
+    Tk, d = x_perm.shape
+    E, dff, _ = W1.shape
+    if y_perm is None:
+        y_perm = torch.empty((Tk, d), dtype=x_perm.dtype, device=x_perm.device)
+    _check("moe_expert_ffn", lib().moe_expert_ffn(_p(x_perm), _p(offsets), _p(W1), _p(W3), _p(W2), _p(y_perm), Tk,
+                                                  d, dff, E, _dtype(x_perm), _stream(stream)))
+    return y_perm
+
+
+def moe_expert_ffn_ws(x_perm, offsets, W1, W3, W2, h_perm=None, y_perm=None, stream=None):
+    """Steps a4 + a5 on caller scratch h_perm[Tk,dff]: returns (h_perm, y_perm)."""
     _dev(x_perm, offsets, W1, W3, W2, h_perm, y_perm)
     Tk, d = x_perm.shape
     E, dff, _ = W1.shape
@@ -203,9 +216,10 @@ def moe_expert_ffn(x_perm, offsets, W1, W3, W2, h_perm=None, y_perm=None, stream
         h_perm = torch.empty((Tk, dff), dtype=x_perm.dtype, device=x_perm.device)
     if y_perm is None:
         y_perm = torch.empty((Tk, d), dtype=x_perm.dtype, device=x_perm.device)
-    _check("moe_expert_ffn", lib().moe_expert_ffn(_p(x_perm), _p(offsets), _p(W1), _p(W3), _p(W2), _p(h_perm),
-                                                  _p(y_perm), Tk, d, dff, E, _dtype(x_perm), _stream(stream)))
-    return y_perm
+    _check("moe_expert_ffn_ws", lib().moe_expert_ffn_ws(_p(x_perm), _p(offsets), _p(W1), _p(W3), _p(W2),
+                                                        _p(h_perm), _p(y_perm), Tk, d, dff, E, _dtype(x_perm),
+                                                        _stream(stream)))
+    return h_perm, y_perm
 
 
 def moe_combine(y_perm, slot_pos, topk_w, T, residual=None, out=None, stream=None):
@@ -221,8 +235,8 @@ def moe_combine(y_perm, slot_pos, topk_w, T, residual=None, out=None, stream=Non
 
 
 # ------------------------------------------------------------------ whole layer
-def moe_forward_workspace_bytes(T, d, dff, E, k, dtype=MOE_DTYPE_BF16) -> int:
-    return int(lib().moe_forward_workspace_bytes(T, d, dff, E, k, dtype))
+def moe_workspace_bytes(T, d, dff, E, k, dtype=MOE_DTYPE_BF16) -> int:
+    return int(lib().moe_workspace_bytes(T, d, dff, E, k, dtype))
 
 
 def workspace_views(ws, T, d, dff, E, k, dtype=MOE_DTYPE_BF16):
@@ -247,7 +261,7 @@ def workspace_views(ws, T, d, dff, E, k, dtype=MOE_DTYPE_BF16):
 
 def workspace(T, d, dff, E, k, dtype=MOE_DTYPE_BF16, device="cuda", host=False):
     """A uint8 device tensor big enough for moe_forward_ws (or moe_forward_host)."""
-    fn = lib().moe_forward_host_workspace_bytes if host else lib().moe_forward_workspace_bytes
+    fn = lib().moe_forward_host_workspace_bytes if host else lib().moe_workspace_bytes
     return torch.empty(max(int(fn(T, d, dff, E, k, dtype)), 256), dtype=torch.uint8, device=device)
 
 

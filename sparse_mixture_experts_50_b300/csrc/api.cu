@@ -32,7 +32,8 @@ DevInfo g_dev[64];
 
 }  // namespace
 
-int make_ctx(const void* dev_ptr, Ctx* ctx) {
+int make_ctx(const void* dev_ptr, Ctx* ctx, int* prev_device) {
+  *prev_device = -1;
   int dev = -1;
   if (dev_ptr != nullptr) {
     cudaPointerAttributes a;
@@ -47,7 +48,10 @@ int make_ctx(const void* dev_ptr, Ctx* ctx) {
   if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ECUDA;
   if (dev < 0) dev = cur;
   if (dev >= 64) return MOE_EUNSUPPORTED;
-  if (dev != cur && cudaSetDevice(dev) != cudaSuccess) return MOE_ECUDA;
+  if (dev != cur) {
+    if (cudaSetDevice(dev) != cudaSuccess) return MOE_ECUDA;
+    *prev_device = cur;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   DevInfo& d = g_dev[dev];
   if (!d.init) {
@@ -256,8 +260,9 @@ int forward_alloc(const void* x, const void* gamma, float eps, const void* Wg, c
                   const void* W2, void* out, int T, int d, int dff, int E, int k, int dtype, cudaStream_t s) {
   MOE_TRY(check_forward(x, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype));
   if (T == 0) return MOE_OK;
-  Ctx c;
-  MOE_TRY(make_ctx(out, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(out));
+  const Ctx& c = scope.ctx();
   const size_t bytes = ws_layout(T, d, dff, E, k, dtype).total;
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
@@ -288,8 +293,9 @@ int forward_w8(const void* x, const void* Wg, const W8Weights& w8, void* out, in
     return MOE_EINVAL;
   MOE_TRY(check_w8(w8));
   if (!alloc && (ws == nullptr || !aligned(ws, 256))) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(out, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(out));
+  const Ctx& c = scope.ctx();
   if (!alloc) {
     return forward_impl(x, nullptr, 0.0f, Wg, nullptr, nullptr, nullptr, out, T, d, dff, E, k, MOE_DTYPE_BF16, ws,
                         ws_bytes, c, s, &w8);
@@ -430,8 +436,9 @@ int moe_router_topk(const void* x, const void* Wg, int T, int d, int E, int k, i
   if (!aligned(x, 16) || !aligned(Wg, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
       !aligned(logits_opt, 4))
     return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(topk_idx, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(topk_idx));
+  const Ctx& c = scope.ctx();
   return launch_rc(launch_router(x, Wg, T, d, E, k, topk_idx, topk_w, logits_opt, dtype, c, stream));
 }
 
@@ -440,8 +447,9 @@ int moe_rmsnorm(const void* x, const void* gamma, float eps, void* xn, int T, in
   MOE_TRY(check_eps(eps));
   if (T == 0) return MOE_OK;
   if (!x || !gamma || !xn || !aligned(x, 16) || !aligned(gamma, 16) || !aligned(xn, 16)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(xn, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(xn));
+  const Ctx& c = scope.ctx();
   return launch_rc(launch_rmsnorm(x, gamma, eps, xn, T, d, dtype, c, stream));
 }
 
@@ -454,8 +462,9 @@ int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int
   if (!aligned(x, 16) || !aligned(x_perm, 16) || !aligned(topk_idx, 4) || !aligned(counts, 4) ||
       !aligned(offsets, 4) || !aligned(row_src, 4) || !aligned(slot_pos, 4))
     return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(offsets, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(offsets));
+  const Ctx& c = scope.ctx();
   const int Tk = T * k;
   MOE_TRY(launch_rc(launch_dispatch(topk_idx, Tk, E, k, counts, offsets, row_src, slot_pos, c, stream)));
   if (Tk == 0) return MOE_OK;
@@ -469,8 +478,9 @@ int moe_expert_gate_up(const void* x_perm, const int32_t* offsets, const void* W
   const void* ptrs[] = {x_perm, offsets, W1, W3, h_perm};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(h_perm, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(h_perm));
+  const Ctx& c = scope.ctx();
   return ffn_gate_up(x_perm, offsets, W1, W3, h_perm, Tk, d, dff, E, dtype, c, stream);
 }
 
@@ -481,15 +491,36 @@ int moe_expert_down(const void* h_perm, const int32_t* offsets, const void* W2, 
   const void* ptrs[] = {h_perm, offsets, W2, y_perm};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(y_perm, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(y_perm));
+  const Ctx& c = scope.ctx();
   return ffn_down(h_perm, offsets, W2, y_perm, Tk, d, dff, E, dtype, c, stream);
 }
 
-int moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, const void* W2,
-                   void* h_perm, void* y_perm, int Tk, int d, int dff, int E, int dtype, moe_stream_t stream) {
+int moe_expert_ffn_ws(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, const void* W2,
+                      void* h_perm, void* y_perm, int Tk, int d, int dff, int E, int dtype, moe_stream_t stream) {
   MOE_TRY(moe_expert_gate_up(x_perm, offsets, W1, W3, h_perm, Tk, d, dff, E, dtype, stream));
   return moe_expert_down(h_perm, offsets, W2, y_perm, Tk, d, dff, E, dtype, stream);
+}
+
+int moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, const void* W2,
+                   void* y_perm, int Tk, int d, int dff, int E, int dtype, moe_stream_t stream) {
+  MOE_TRY(check_ffn(Tk, d, dff, E, dtype));
+  if (Tk == 0) return MOE_OK;
+  const void* ptrs[] = {x_perm, offsets, W1, W3, W2, y_perm};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
+  CtxScope scope;
+  MOE_TRY(scope.init(y_perm));
+  void* h = nullptr;
+  if (cudaMallocAsync(&h, static_cast<size_t>(Tk) * dff * esize(dtype), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ENOMEM;
+  }
+  const int rc = moe_expert_ffn_ws(x_perm, offsets, W1, W3, W2, h, y_perm, Tk, d, dff, E, dtype, stream);
+  const cudaError_t fe = cudaFreeAsync(h, stream);
+  if (rc != MOE_OK) return rc;
+  return fe == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 
 int moe_combine(const void* y_perm, const int32_t* slot_pos, const float* topk_w, const void* residual_opt, void* out,
@@ -500,8 +531,9 @@ int moe_combine(const void* y_perm, const int32_t* slot_pos, const float* topk_w
   if (!aligned(y_perm, 16) || !aligned(out, 16) || !aligned(residual_opt, 16) || !aligned(slot_pos, 4) ||
       !aligned(topk_w, 4))
     return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(out, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(out));
+  const Ctx& c = scope.ctx();
   return launch_rc(launch_combine(y_perm, slot_pos, topk_w, residual_opt, out, T, d, k, dtype, c, stream));
 }
 
@@ -515,7 +547,7 @@ int moe_forward_workspace_offsets(int T, int d, int dff, int E, int k, int dtype
   return MOE_OK;
 }
 
-size_t moe_forward_workspace_bytes(int T, int d, int dff, int E, int k, int dtype) {
+size_t moe_workspace_bytes(int T, int d, int dff, int E, int k, int dtype) {
   if (check_tokens(T, d, E, k, dtype) != MOE_OK || dff <= 0) return 0;
   return ws_layout(T, d, dff, E, k, dtype).total;
 }
@@ -532,8 +564,9 @@ int moe_forward_ws(const void* x, const void* Wg, const void* W1, const void* W3
   MOE_TRY(check_forward(x, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype));
   if (T == 0) return MOE_OK;
   if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(out, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(out));
+  const Ctx& c = scope.ctx();
   return forward_impl(x, nullptr, 0.0f, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype, workspace, workspace_bytes, c,
                       stream);
 }
@@ -545,8 +578,9 @@ int moe_forward_train_ws(const void* x, const void* Wg, const void* W1, const vo
   if (T == 0) return MOE_OK;
   if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
   if (keep == nullptr || !aligned(keep, 16)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(out, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(out));
+  const Ctx& c = scope.ctx();
   return forward_impl(x, nullptr, 0.0f, Wg, W1, W3, W2, out, T, d, dff, E, k, MOE_DTYPE_BF16, workspace,
                       workspace_bytes, c, stream, nullptr, nullptr, keep);
 }
@@ -569,8 +603,9 @@ int moe_block_forward_ws(const void* x, const void* gamma, float eps, const void
   if (T == 0) return MOE_OK;
   if (gamma == nullptr || !aligned(gamma, 16)) return MOE_EINVAL;
   if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(out, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(out));
+  const Ctx& c = scope.ctx();
   return forward_impl(x, gamma, eps, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype, workspace, workspace_bytes, c,
                       stream);
 }
@@ -583,7 +618,7 @@ int moe_block_forward(const void* x, const void* gamma, float eps, const void* W
 }
 
 size_t moe_forward_host_workspace_bytes(int T, int d, int dff, int E, int k, int dtype) {
-  const size_t base = moe_forward_workspace_bytes(T, d, dff, E, k, dtype);
+  const size_t base = moe_workspace_bytes(T, d, dff, E, k, dtype);
   if (base == 0) return 0;
   const size_t act = al256(static_cast<size_t>(T) * d * esize(dtype));
   return base + 2 * act;
@@ -597,9 +632,10 @@ int moe_forward_host(const void* x_host, const void* Wg, const void* W1, const v
   if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
   const size_t need = moe_forward_host_workspace_bytes(T, d, dff, E, k, dtype);
   if (workspace_bytes < need) return MOE_ENOMEM;
-  Ctx c;
-  MOE_TRY(make_ctx(Wg, &c));
-  const size_t base = moe_forward_workspace_bytes(T, d, dff, E, k, dtype);
+  CtxScope scope;
+  MOE_TRY(scope.init(Wg));
+  const Ctx& c = scope.ctx();
+  const size_t base = moe_workspace_bytes(T, d, dff, E, k, dtype);
   const size_t act_bytes = static_cast<size_t>(T) * d * esize(dtype);
   uint8_t* x_dev = static_cast<uint8_t*>(workspace) + base;
   uint8_t* out_dev = x_dev + al256(act_bytes);
@@ -625,8 +661,9 @@ int moe_forward_ex(const void* x, const void* gamma_opt, float eps, const void* 
   if (w8) MOE_TRY(check_w8(q));
   if (gamma_opt != nullptr && !aligned(gamma_opt, 16)) return MOE_EINVAL;
   if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(out, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(out));
+  const Ctx& c = scope.ctx();
   return forward_impl(x, gamma_opt, eps, Wg, W1, W3, W2, out, T, d, dff, E, k, dtype, workspace, workspace_bytes, c,
                       stream, w8 ? &q : nullptr, events);
 }
@@ -636,8 +673,9 @@ int moe_quantize_int8(const void* W, int rows, int cols, int8_t* q, float* scale
   if (cols % 8 != 0) return MOE_EUNSUPPORTED;
   if (rows == 0) return MOE_OK;
   if (!W || !q || !scale || !aligned(W, 16) || !aligned(q, 16) || !aligned(scale, 4)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(q, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(q));
+  const Ctx& c = scope.ctx();
   return launch_rc(launch_quantize_int8(W, rows, cols, q, scale, c, stream));
 }
 
@@ -649,8 +687,9 @@ int moe_expert_gate_up_w8(const void* x_perm, const int32_t* offsets, const int8
   const void* ptrs[] = {x_perm, offsets, W1q, W1s, W3q, W3s, h_perm};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(h_perm, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(h_perm));
+  const Ctx& c = scope.ctx();
   return launch_w8_gate_up(x_perm, offsets, W1q, W1s, W3q, W3s, h_perm, Tk, d, dff, E, c, stream);
 }
 
@@ -661,8 +700,9 @@ int moe_expert_down_w8(const void* h_perm, const int32_t* offsets, const int8_t*
   const void* ptrs[] = {h_perm, offsets, W2q, W2s, y_perm};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned(p, 16)) return MOE_EINVAL;
-  Ctx c;
-  MOE_TRY(make_ctx(y_perm, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(y_perm));
+  const Ctx& c = scope.ctx();
   return launch_w8_down(h_perm, offsets, W2q, W2s, y_perm, Tk, d, dff, E, c, stream);
 }
 
@@ -694,8 +734,9 @@ int moe_backward_ws(const void* dout, const void* x, const void* Wg, const void*
   if (T == 0) return MOE_OK;
   if (workspace == nullptr || !aligned(workspace, 256)) return MOE_EINVAL;
   if (workspace_bytes < bwd_layout(T, d, dff, E, k).total) return MOE_ENOMEM;
-  Ctx c;
-  MOE_TRY(make_ctx(dx, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(dx));
+  const Ctx& c = scope.ctx();
   return backward_impl(dout, x, Wg, W1, W3, W2, saved, keep, dx, dWg, dW1, dW3, dW2, T, d, dff, E, k, workspace,
                        c, stream);
 }
@@ -706,8 +747,9 @@ int moe_backward(const void* dout, const void* x, const void* Wg, const void* W1
   MOE_TRY(check_backward(dout, x, Wg, W1, W3, W2, saved, saved_bytes, keep, dx, dWg, dW1, dW3, dW2, T, d, dff, E,
                          k));
   if (T == 0) return MOE_OK;
-  Ctx c;
-  MOE_TRY(make_ctx(dx, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(dx));
+  const Ctx& c = scope.ctx();
   const size_t bytes = bwd_layout(T, d, dff, E, k).total;
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
@@ -728,15 +770,17 @@ int moe_get_device_status(moe_stream_t stream, int* status, int reset) {
   int cur = 0;
   if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ECUDA;
   if (dev != cur && cudaSetDevice(dev) != cudaSuccess) return MOE_ECUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ECUDA;
+  int rc = MOE_OK;
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return MOE_ECUDA;
-  if (reset) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess || cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) {
+    rc = MOE_ECUDA;
+  } else if (reset) {
     const int z = 0;
-    if (cudaMemcpyToSymbol(g_status, &z, sizeof(int)) != cudaSuccess) return MOE_ECUDA;
+    if (cudaMemcpyToSymbol(g_status, &z, sizeof(int)) != cudaSuccess) rc = MOE_ECUDA;
   }
-  *status = v;
-  return MOE_OK;
+  if (dev != cur) cudaSetDevice(cur);  // the caller's current device again
+  if (rc == MOE_OK) *status = v;
+  return rc;
 }
 
 }  // extern "C"
@@ -782,8 +826,9 @@ extern "C" int moe_forward_noalloc(const void* x, const void* Wg, const void* W1
   if (T == 0) return MOE_OK;
   const size_t need = ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16).total;
   if (need > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ENOMEM;
-  Ctx c;
-  MOE_TRY(make_ctx(out, &c));
+  CtxScope scope;
+  MOE_TRY(scope.init(out));
+  const Ctx& c = scope.ctx();
   void* scratch = nullptr;
   MOE_TRY(noalloc_scratch(c.device, &scratch));
   // Every step writes all the scratch it later reads (indices, weights,

@@ -23,8 +23,33 @@ struct Ctx {
 
 // Sets the calling thread's current device to the one owning `dev_ptr`
 // (or keeps the current device if the pointer is not a device pointer) and
-// fills `ctx`.  Returns MOE_OK or MOE_ECUDA.
-int make_ctx(const void* dev_ptr, Ctx* ctx);
+// fills `ctx`; `*prev_device` receives the device that was current before
+// (-1 if it could not be read).  Returns MOE_OK or MOE_ECUDA.
+int make_ctx(const void* dev_ptr, Ctx* ctx, int* prev_device);
+
+// What every entry point holds for its call: the context of the device that
+// owns its operands, made current for the call, and the caller's current
+// device, made current again when the entry point returns.
+class CtxScope {
+ public:
+  CtxScope() = default;
+  CtxScope(const CtxScope&) = delete;
+  CtxScope& operator=(const CtxScope&) = delete;
+  ~CtxScope() {
+    if (prev_ >= 0 && switched_) cudaSetDevice(prev_);
+  }
+  int init(const void* dev_ptr) {
+    const int rc = make_ctx(dev_ptr, &ctx_, &prev_);
+    switched_ = prev_ >= 0;
+    return rc;
+  }
+  const Ctx& ctx() const { return ctx_; }
+
+ private:
+  Ctx ctx_ = {};
+  int prev_ = -1;
+  bool switched_ = false;
+};
 
 // Records `code` in the device status word unless one is already recorded.
 __device__ __forceinline__ void record_status(int* status, int code) {

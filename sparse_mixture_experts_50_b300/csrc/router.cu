@@ -83,8 +83,9 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __rest
     }
     if (!valid) continue;
     // Top-k, identical in every thread of the token.  Strict '>' over
-    // ascending e keeps the lower index on equal logits; a NaN never wins
-    // but a slot is always filled.
+    // ascending e keeps the lower index on equal logits.  A NaN logit is
+    // taken only when no other expert is left: any number replaces a NaN
+    // best, and no comparison with a NaN candidate succeeds.
     uint64_t taken = 0;
     float sel_l[8];
     int sel_i[8];
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __rest
         int bi = -1;
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) {
-          if (e < E && !((taken >> e) & 1ull) && (bi < 0 || acc[e] > best)) {
+          if (e < E && !((taken >> e) & 1ull) && (bi < 0 || acc[e] > best || (best != best && acc[e] == acc[e]))) {
             best = acc[e];
             bi = e;
           }
@@ -129,9 +130,11 @@ __global__ void __launch_bounds__(kThreads) router_topk_kernel(const TIn* __rest
       w[static_cast<size_t>(t) * k + tt] = my_e / sum;
     }
     if (logits != nullptr) {
+      // Every thread of the token holds all E logits; thread tt writes
+      // experts tt, tt + TPT, ... (E may exceed the group's 32 threads).
 #pragma unroll
       for (int e = 0; e < EMAX; ++e) {
-        if (e < E && e == tt) logits[static_cast<size_t>(t) * E + e] = acc[e];
+        if (e < E && e % TPT == tt) logits[static_cast<size_t>(t) * E + e] = acc[e];
       }
     }
   }

@@ -187,6 +187,92 @@ def pin_dispatch_brute_force(o):
             assert slot_pos[t * k + j] == p
 
 
+def _segments(counts):
+    """Offsets of consecutive expert segments with the given row counts, and
+    the expert of every row, by plain loops."""
+    offsets, owner = [0], []
+    for e, n in enumerate(counts):
+        offsets.append(offsets[-1] + n)
+        owner += [e] * n
+    return offsets, owner
+
+
+def pin_gate_up_projection_brute_force(o):
+    """Grouped gate/up: each row meets its own expert's W1 and W3 only, by
+    pure-Python loops; empty segments and a segment at the end included."""
+    r = _rng(34)
+    counts = [2, 0, 3, 1, 0]
+    offsets, owner = _segments(counts)
+    E, F, d = len(counts), 4, 3
+    x = r.standard_normal((offsets[-1], d))
+    W1, W3 = r.standard_normal((E, F, d)), r.standard_normal((E, F, d))
+    got = o.gate_up_projection(x, offsets, W1, W3)
+    assert got.shape == (offsets[-1], F)
+    for p, e in enumerate(owner):
+        for f in range(F):
+            want = _py_silu(_py_dot(x[p], W1[e][f])) * _py_dot(x[p], W3[e][f])
+            assert abs(got[p, f] - want) < 1e-13 * max(1.0, abs(want)), (p, f)
+
+
+def pin_down_projection_brute_force(o):
+    """Grouped down projection: y[p][c] = sum_f h[p][f] W2[e][c][f] with e the
+    expert owning row p, by pure-Python loops (W2 is [E, d, F]: output
+    channel first)."""
+    r = _rng(35)
+    counts = [0, 3, 2, 0, 1]
+    offsets, owner = _segments(counts)
+    E, F, d = len(counts), 5, 3
+    h = r.standard_normal((offsets[-1], F))
+    W2 = r.standard_normal((E, d, F))
+    got = o.down_projection(h, offsets, W2)
+    assert got.shape == (offsets[-1], d)
+    for p, e in enumerate(owner):
+        for c in range(d):
+            want = _py_dot(h[p], W2[e][c])
+            assert abs(got[p, c] - want) < 1e-13 * max(1.0, abs(want)), (p, c)
+
+
+def pin_combine_brute_force(o):
+    """Combine: out[t] = sum_j w[t][j] y[slot_pos[t*k+j]] (+ residual[t]), by
+    pure-Python loops over tokens and slots, with a shuffled slot_pos."""
+    r = _rng(36)
+    T, k, d = 5, 3, 4
+    y = r.standard_normal((T * k, d))
+    pos = r.permutation(T * k)
+    w = r.uniform(0.1, 1.0, (T, k))
+    res = r.standard_normal((T, d))
+    for residual in (None, res):
+        got = o.combine(y, pos, w, residual)
+        for t in range(T):
+            for c in range(d):
+                terms = [w[t][j] * y[pos[t * k + j]][c] for j in range(k)]
+                if residual is not None:
+                    terms.append(residual[t][c])
+                want = math.fsum(terms)
+                assert abs(got[t, c] - want) < 1e-13 * max(1.0, abs(want)), (t, c)
+
+
+def pin_grouped_steps_compose_to_layer(o):
+    """dispatch -> gather -> gate_up_projection -> down_projection -> combine
+    with the router's (w, idx) gives the layer by brute force: the grouped
+    steps are the layer of section 05, reordered."""
+    L = _tiny_layer(61, T=14, d=6, F=5)
+    k = 2
+    w, idx, _ = o.router(L["x"], L["Wg"], k)
+    counts, offsets, row_src, slot_pos = o.dispatch(idx, 8)
+    h = o.gate_up_projection(L["x"][row_src], offsets, L["W1"], L["W3"])
+    y = o.down_projection(h, offsets, L["W2"])
+    out = o.combine(y, slot_pos, w)
+    for t in range(14):
+        lg = [_py_dot(L["x"][t], L["Wg"][e]) for e in range(8)]
+        i0, i1 = sorted(max(itertools.combinations(range(8), 2), key=lambda s: lg[s[0]] + lg[s[1]]),
+                        key=lambda e: -lg[e])
+        w0 = 1.0 / (1.0 + math.exp(lg[i1] - lg[i0]))
+        y0 = _py_swiglu(L["x"][t], L["W1"][i0], L["W3"][i0], L["W2"][i0])
+        y1 = _py_swiglu(L["x"][t], L["W1"][i1], L["W3"][i1], L["W2"][i1])
+        assert np.allclose(out[t], [w0 * a + (1.0 - w0) * b for a, b in zip(y0, y1)], rtol=1e-12, atol=1e-14), t
+
+
 def pin_swiglu_hidden_textbook(o):
     """The hidden activation silu(W1 x) * (W3 x) by pure-Python loops."""
     r = _rng(33)

@@ -32,6 +32,39 @@ def test_header_declares_the_layer_steps():
         assert n in names
 
 
+# The boundary the layer's scope table names, with each call's argument count
+# (pointers, sizes, dtype and stream, in that table's order).
+SURVEY_BOUNDARY = {
+    "moe_router_topk": 11,       # x, Wg, T, d, E, k, topk_idx, topk_w, logits_opt, dtype, stream
+    "moe_permute": 13,           # x, topk_idx, T, d, E, k, counts, offsets, row_src, slot_pos, x_perm, dtype, stream
+    "moe_expert_ffn": 12,        # x_perm, offsets, W1, W3, W2, y_perm, Tk, d, dff, E, dtype, stream
+    "moe_combine": 10,           # y_perm, slot_pos, topk_w, residual_opt, out, T, d, k, dtype, stream
+    "moe_forward": 12,           # x, Wg, W1, W3, W2, out, T, d, dff, E, k, stream
+    "moe_forward_f32": 12,
+    "moe_block_forward": 14,     # x, gamma, eps, then moe_forward's arguments
+    "moe_workspace_bytes": 6,    # T, d, dff, E, k, dtype
+}
+
+
+def test_boundary_names_and_arities():
+    names = declared_functions()
+    for n, nargs in SURVEY_BOUNDARY.items():
+        assert n in names, f"include/moe.h does not declare {n}"
+        assert len(B.SIGNATURES[n][1]) == nargs, (n, len(B.SIGNATURES[n][1]), nargs)
+    assert B.SIGNATURES["moe_workspace_bytes"][0] is ctypes.c_size_t
+
+
+def test_expert_ffn_validation(lib):
+    """moe_expert_ffn checks its arguments before it allocates anything."""
+    f = lib.moe_expert_ffn
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 10, 96, 128, 8, 1, NULL) == B.MOE_EUNSUPPORTED  # d % 64
+    assert f(FAKE, NULL, FAKE, FAKE, FAKE, FAKE, 10, 128, 128, 8, 1, NULL) == B.MOE_EINVAL      # null offsets
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 8, 10, 128, 128, 8, 1, NULL) == B.MOE_EINVAL  # misaligned out
+    assert f(NULL, NULL, NULL, NULL, NULL, NULL, 0, 128, 128, 8, 1, NULL) == B.MOE_OK           # Tk = 0
+    g = lib.moe_expert_ffn_ws
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, 10, 128, 128, 8, 1, NULL) == B.MOE_EINVAL  # null h_perm
+
+
 def test_every_declared_symbol_is_exported_and_bound(lib):
     names = declared_functions()
     assert len(names) >= 19
@@ -96,11 +129,11 @@ def test_forward_validation(lib):
 
 def test_workspace_bytes(lib):
     T, d, F, E, k = 8192, 4096, 14336, 8, 2
-    n = lib.moe_forward_workspace_bytes(T, d, F, E, k, 1)
+    n = lib.moe_workspace_bytes(T, d, F, E, k, 1)
     # x_perm + h + y + xn (bf16) plus index arrays
     act = T * k * d * 2 + T * k * F * 2 + T * k * d * 2 + T * d * 2
     assert act < n < act + 1 << 20
-    assert lib.moe_forward_workspace_bytes(-1, d, F, E, k, 1) == 0
+    assert lib.moe_workspace_bytes(-1, d, F, E, k, 1) == 0
     h = lib.moe_forward_host_workspace_bytes(T, d, F, E, k, 1)
     assert h == n + 2 * T * d * 2
 
@@ -117,7 +150,7 @@ def test_w8_workspace_bytes(lib):
     each matrix 256-byte aligned) exactly when the experts average at least
     512 routed rows."""
     d, F, E, k = 4096, 14336, 8, 2
-    base = lambda T: lib.moe_forward_workspace_bytes(T, d, F, E, k, B.MOE_DTYPE_BF16)
+    base = lambda T: lib.moe_workspace_bytes(T, d, F, E, k, B.MOE_DTYPE_BF16)
     wide = 3 * ((E * F * d * 2 + 255) // 256 * 256)
     assert lib.moe_forward_w8_workspace_bytes(16, d, F, E, k) == base(16)
     assert lib.moe_forward_w8_workspace_bytes(4096, d, F, E, k) == base(4096) + wide
@@ -136,7 +169,7 @@ def test_training_entry_validation(lib):
     assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 8, T, d, F, E, k, FAKE, 1 << 30, NULL) == B.MOE_EINVAL
     assert fwd(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, d, F, E, k, NULL, 0, NULL) == B.MOE_OK
     bwd = lib.moe_backward_ws
-    saved = lib.moe_forward_workspace_bytes(T, d, F, E, k, B.MOE_DTYPE_BF16)
+    saved = lib.moe_workspace_bytes(T, d, F, E, k, B.MOE_DTYPE_BF16)
     need = lib.moe_backward_workspace_bytes(T, d, F, E, k)
     assert need > 0
 

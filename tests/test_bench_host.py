@@ -54,3 +54,42 @@ def test_ncu_traffic_only_on_matching_source(name, tmp_path, monkeypatch):
     assert got is None or got > 0
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0000000000000000")
     assert bench.ncu_traffic(name) is None
+
+
+class _FakeLayer:
+    """A stand-in for bench.Layer whose routing and output are given."""
+
+    def __init__(self, wl, idx, out):
+        import torch
+        self.wl = wl
+        self.idx = torch.from_numpy(idx.astype("int32"))
+        self.out = torch.from_numpy(out)
+
+
+def test_accuracy_accounting_on_planted_results():
+    """bench.accuracy counts near ties and clear-token routing differences and
+    scores outputs: the oracle's own result scores 0; one clear token routed
+    to other experts is counted."""
+    import numpy as np
+    import oracle.moe_oracle as O
+    wl = mw.Workload("acc_probe", 40, 32, 48, 8, 2, "f32", "inv_sqrt")
+    t = mw.make_inputs(wl)
+    out, w, idx, logits = O.moe_forward(t["x"], t["Wg"], t["W1"], t["W3"], t["W2"], wl.k)
+    top = -np.sort(-logits, axis=1)[:, :3]
+    near = int(np.sum(np.any(top[:, :-1] - top[:, 1:] < 1e-3, axis=1)))
+    a = bench.accuracy(_FakeLayer(wl, idx, out), t, sample=40)
+    assert a["near_tie_tokens"] == near
+    assert a["clear_tokens_routed_differently"] == 0 and a["near_tie_routed_differently"] == 0
+    assert a["rel_l2"] < 1e-15 and a["scored_tokens"] == 40
+    bad = idx.copy()
+    clear = int(np.nonzero(~np.any(top[:, :-1] - top[:, 1:] < 1e-3, axis=1))[0][0])
+    bad[clear] = [e for e in range(8) if e not in idx[clear]][:2]
+    a = bench.accuracy(_FakeLayer(wl, bad, out), t, sample=40)
+    assert a["clear_tokens_routed_differently"] == 1
+
+
+def test_targets_of():
+    res = {"decode": {"bound": "hbm", "layer_roofline_frac": 0.9}, "block": {"bound": "tensor",
+                                                                           "layer_roofline_frac": 0.55}}
+    t = bench.targets_of(res)
+    assert t["decode"]["met"] and not t["block"]["met"] and "skewed" not in t

@@ -91,6 +91,39 @@ def test_router_ties_and_k(B):
         check_routing(to_np(idx), to_np(w), ora_idx, ora_w, logits, k)
 
 
+def test_router_logits_wide_e_large_batch(B):
+    """E=64 at a batch large enough for one warp per token (32 threads per
+    token, fewer than E): every logit is written and matches the oracle."""
+    r = np.random.default_rng(29)
+    T, d, E, k = 12000, 128, 64, 2
+    x = torch.from_numpy(r.standard_normal((T, d))).to(torch.bfloat16)
+    Wg = torch.from_numpy(r.standard_normal((E, d)) * 0.05).to(torch.bfloat16)
+    lg = torch.full((T, E), float("nan"), dtype=torch.float32, device=DEV)
+    idx, w = B.moe_router_topk(dev(x), dev(Wg), k, logits=lg)
+    status_ok(B)
+    ora_w, ora_idx, logits = O.router(x, Wg, k)
+    got = to_np(lg)
+    assert np.all(np.isfinite(got)), "logits left unwritten"
+    assert np.max(np.abs(got - logits)) < 2e-4
+    check_routing(to_np(idx), to_np(w), ora_idx, ora_w, logits, k)
+
+
+def test_router_nan_logit_not_chosen(B):
+    """A NaN logit (expert 0 here) is never picked while another expert is
+    left; the routing among the others matches the oracle's over them."""
+    r = np.random.default_rng(31)
+    T, d, E, k = 50, 64, 8, 2
+    x = torch.from_numpy(r.standard_normal((T, d))).float()
+    Wg = torch.from_numpy(r.standard_normal((E, d)) * 0.1).float()
+    Wg[0, 3] = float("nan")
+    idx, w = B.moe_router_topk(dev(x), dev(Wg), k)
+    status_ok(B)
+    gi = to_np(idx)
+    assert not np.any(gi == 0)
+    ora_w, ora_idx, logits = O.router(x, Wg[1:], k)
+    check_routing(gi - 1, to_np(w), ora_idx, ora_w, logits, k)
+
+
 # ------------------------------------------------------------------ dispatch
 @pytest.mark.parametrize("name", SMALL)
 def test_permute(B, name):
@@ -147,34 +180,34 @@ def segment_inputs(name):
     return wl, t, offsets, x_perm
 
 
-def hidden_ref(x_perm, offsets, W1, W3):
-    out = np.zeros((x_perm.shape[0], W1.shape[1]))
-    for e in range(W1.shape[0]):
-        a, b = offsets[e], offsets[e + 1]
-        if b > a:
-            out[a:b] = O.swiglu_hidden(x_perm[a:b], W1[e], W3[e])
-    return out
-
-
-def down_ref(h, offsets, W2):
-    out = np.zeros((h.shape[0], W2.shape[1]))
-    for e in range(W2.shape[0]):
-        a, b = offsets[e], offsets[e + 1]
-        if b > a:
-            out[a:b] = O.f64(h[a:b]) @ O.f64(W2[e]).T
-    return out
-
-
 @pytest.mark.parametrize("name", SMALL)
 def test_expert_gate_up_and_down(B, name):
     wl, t, offsets, x_perm = segment_inputs(name)
     off = dev(torch.from_numpy(offsets).int())
     h = B.moe_expert_gate_up(dev(x_perm), off, dev(t["W1"]), dev(t["W3"]))
     status_ok(B)
-    check_close(to_np(h), hidden_ref(x_perm, offsets, t["W1"], t["W3"]), wl.dtype, f"{name} h")
+    check_close(to_np(h), O.gate_up_projection(x_perm, offsets, t["W1"], t["W3"]), wl.dtype, f"{name} h")
     y = B.moe_expert_down(h, off, dev(t["W2"]))
     status_ok(B)
-    check_close(to_np(y), down_ref(h.cpu(), offsets, t["W2"]), wl.dtype, f"{name} y")
+    check_close(to_np(y), O.down_projection(h.cpu(), offsets, t["W2"]), wl.dtype, f"{name} y")
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "small_ragged", "small_f32"])
+def test_expert_ffn_entry_points(B, name):
+    """moe_expert_ffn (pool scratch) and moe_expert_ffn_ws (caller scratch)
+    against the oracle's grouped steps, and bit for bit against the two
+    single-step calls."""
+    wl, t, offsets, x_perm = segment_inputs(name)
+    off = dev(torch.from_numpy(offsets).int())
+    g = [dev(t[n]) for n in ("W1", "W3", "W2")]
+    y = B.moe_expert_ffn(dev(x_perm), off, *g)
+    h_ws, y_ws = B.moe_expert_ffn_ws(dev(x_perm), off, *g)
+    h1 = B.moe_expert_gate_up(dev(x_perm), off, g[0], g[1])
+    y1 = B.moe_expert_down(h1, off, g[2])
+    status_ok(B)
+    assert torch.equal(y, y1) and torch.equal(y_ws, y1) and torch.equal(h_ws, h1)
+    ref = O.down_projection(O.gate_up_projection(x_perm, offsets, t["W1"], t["W3"]), offsets, t["W2"])
+    check_close(to_np(y), ref, wl.dtype, f"{name} expert_ffn")
 
 
 @pytest.mark.parametrize("counts", [
@@ -203,8 +236,8 @@ def test_expert_tiles(B, counts, dtype):
     h = B.moe_expert_gate_up(dev(x), off, dev(W1), dev(W3))
     y = B.moe_expert_down(h, off, dev(W2))
     status_ok(B)
-    check_close(to_np(h), hidden_ref(x, offsets, W1, W3), dtype, "h")
-    check_close(to_np(y), down_ref(h.cpu(), offsets, W2), dtype, "y")
+    check_close(to_np(h), O.gate_up_projection(x, offsets, W1, W3), dtype, "h")
+    check_close(to_np(y), O.down_projection(h.cpu(), offsets, W2), dtype, "y")
 
 
 # ------------------------------------------------------------------ combine
@@ -219,8 +252,7 @@ def test_combine(B, dtype, res):
     x = torch.from_numpy(r.standard_normal((T, d))).to(tdt)
     out = B.moe_combine(dev(y), dev(slot_pos), dev(w), T, residual=dev(x) if res else None)
     status_ok(B)
-    yy = to_np(y)[slot_pos.numpy().reshape(T, k)]
-    ref = np.einsum("tk,tkd->td", w.double().numpy(), yy) + (to_np(x) if res else 0.0)
+    ref = O.combine(y, slot_pos.numpy(), w.numpy(), x if res else None)
     check_close(to_np(out), ref, dtype, "combine")
     if dtype == "bf16":  # one rounding of the fp32 sum
         assert np.max(np.abs(to_np(out) - ref) / np.maximum(np.abs(ref), 1e-3)) <= 2.0 ** -8 + 1e-6

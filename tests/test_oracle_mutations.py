@@ -266,6 +266,48 @@ def _slice_gate_up_swapped(m):
     m.expert_grad_hidden_unit = lambda xe, doute, we, W1e, W3e, W2e, f: src(xe, doute, we, W3e, W1e, W2e, f)
 
 
+def _down_next_expert(m):
+    """Each segment multiplied by the next expert's W2 (an off-by-one index)."""
+    def down(h, offsets, W2):
+        return m.__dict__["_orig_down"](h, offsets, np.roll(np.asarray(W2), -1, axis=0))
+    m._orig_down = m.down_projection
+    m.down_projection = down
+
+
+def _down_skips_last_segment(m):
+    def down(h, offsets, W2):
+        off = np.array(offsets, copy=True)
+        off[-1] = off[-2]
+        return m.__dict__["_orig_down2"](h, off, W2)
+    m._orig_down2 = m.down_projection
+    m.down_projection = down
+
+
+def _gate_up_grouped_swapped(m):
+    src = m.gate_up_projection
+    m.gate_up_projection = lambda x_perm, offsets, W1, W3: src(x_perm, offsets, W3, W1)
+
+
+def _combine_drops_weight(m):
+    src = m.combine
+    m.combine = lambda y, pos, w, residual=None: src(y, pos, np.ones_like(np.asarray(w, dtype=float)), residual)
+
+
+def _combine_slot_major(m):
+    """slot_pos read as [k, T] instead of [T, k]."""
+    src = m.combine
+
+    def comb(y, pos, w, residual=None):
+        T, k = np.asarray(w).shape
+        return src(y, np.asarray(pos).reshape(k, T).T.reshape(-1), w, residual)
+    m.combine = comb
+
+
+def _combine_drops_residual(m):
+    src = m.combine
+    m.combine = lambda y, pos, w, residual=None: src(y, pos, w, None)
+
+
 MUTANTS = {f.__name__[1:]: f for f in [
     _swap_gate_up, _silu_sign, _silu_is_sigmoid, _no_renormalise, _ascending_topk,
     _ties_to_higher_index, _drop_gate_weight, _only_first_slot, _transposed_down,
@@ -274,7 +316,8 @@ MUTANTS = {f.__name__[1:]: f for f in [
     _dispatch_token_not_pair, _hidden_no_gate, _rms32_no_square, _int8_divisor_128, _int8_truncates,
     _int8_ties_away_from_zero, _int8_per_column, _w8_drops_scale, _bwd_silu_grad_is_silu,
     _bwd_silu_grad_drops_term, _bwd_no_softmax_jacobian, _bwd_drops_gate_weight, _bwd_transposed_dw1,
-    _slice_drops_gate_weight, _slice_gate_up_swapped]}
+    _slice_drops_gate_weight, _slice_gate_up_swapped, _down_next_expert, _down_skips_last_segment,
+    _gate_up_grouped_swapped, _combine_drops_weight, _combine_slot_major, _combine_drops_residual]}
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
