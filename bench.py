@@ -199,8 +199,7 @@ class Layer:
             self.W1 = self.W3 = self.W2 = None
             self.w8 = (self.W1q, self.W1s, self.W3q, self.W3s, self.W2q, self.W2s)
         dtype = B.MOE_DTYPE_BF16 if wl.dtype == "bf16" else B.MOE_DTYPE_F32
-        # int8 weights: scratch that also lets large batches widen the codes once per call.
-        self.ws = B.w8_workspace(T, d, F, E, k, device=dev) if wl.w8 else B.workspace(T, d, F, E, k, dtype, device=dev)
+        self.ws = B.workspace(T, d, F, E, k, dtype, device=dev)
         v = B.workspace_views(self.ws, T, d, F, E, k, dtype)
         self.idx, self.w, self.counts, self.offsets = v["idx"], v["w"], v["counts"], v["offsets"]
         self.row_src, self.slot_pos, self.x_perm, self.h, self.y = (v["row_src"], v["slot_pos"], v["x_perm"], v["h"],

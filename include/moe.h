@@ -107,6 +107,18 @@ int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int
                 void* x_perm, int dtype, moe_stream_t stream);
 
 /*
+ * The row copy of step a3 on its own, for moving routed rows between
+ * orders (the expert-parallel layer regroups the rows it received per
+ * expert with it): dst[i] = src[row_idx[i]] for i < n_rows, rows of
+ * row_bytes bytes (a multiple of 16; src and dst 16-byte aligned),
+ * row_idx[n_rows] int32 (device).  An index outside [0, src_rows) is skipped
+ * (its row of dst is left as it was) and sets MOE_EDEVICE in the device
+ * status.
+ */
+int moe_gather_rows(const void* src, int src_rows, const int32_t* row_idx, int n_rows, void* dst,
+                    size_t row_bytes, moe_stream_t stream);
+
+/*
  * Step a4 - grouped gate/up GEMM with the SwiGLU fused into its epilogue
  * (section 04): for expert e and every row p in [offsets[e], offsets[e+1]),
  *   h_perm[p, f] = silu(sum_c x_perm[p,c] W1[e,f,c]) * sum_c x_perm[p,c] W3[e,f,c]
@@ -212,11 +224,9 @@ int moe_block_forward(const void* x, const void* gamma, float eps, const void* W
  *    W1, W3, W2 are then ignored; bf16 only);
  *  - events (NULL, or 5 cudaEvent_t; NULL entries skipped) are recorded on
  *    `stream` before the router, after dispatch, after the gate/up GEMM,
- *    after the down GEMM and after the combine (with int8 weights in the
- *    widened-once form, the widening falls between the second and third).
- * workspace as moe_forward_ws; with int8 weights, as moe_forward_w8_ws (the
- * large-batch form needs moe_forward_w8_workspace_bytes()).  Same results as
- * the corresponding entry point.
+ *    after the down GEMM and after the combine.
+ * workspace as moe_forward_ws (moe_workspace_bytes()).  Same results as the
+ * corresponding entry point.
  */
 int moe_forward_ex(const void* x, const void* gamma_opt, float eps, const void* Wg, const void* W1,
                    const void* W3, const void* W2, const int8_t* W1q, const float* W1s, const int8_t* W3q,
@@ -281,12 +291,11 @@ int moe_expert_down_w8(const void* h_perm, const int32_t* offsets, const int8_t*
  * (256-byte aligned) of at least moe_workspace_bytes(T, d, dff, E, k,
  * MOE_DTYPE_BF16) bytes; the other takes it from cudaMallocAsync on `stream`.
  *
- * Two forms compute the same products (codes times per-row scales, fp32
- * accumulation).  Few rows: the GEMMs widen each weight tile from int8 on the
- * SM.  When the experts average >= 512 routed rows (T*k >= 512*E) and the
- * scratch holds moe_forward_w8_workspace_bytes() (3*E*dff*d*2 bytes more,
- * the alloc form always does), the codes are widened once per call into that
- * scratch and the bf16 GEMMs apply the scales in their epilogue.
+ * The codes are widened to bf16 on the SM (exactly: every code is a bf16
+ * value) straight into the tensor cores' operand memory, and the per-row
+ * scales are applied to the fp32 accumulators; no bf16 copy of the weights
+ * is made, so moe_forward_w8_workspace_bytes() equals moe_workspace_bytes()
+ * of the bf16 layer.
  */
 size_t moe_forward_w8_workspace_bytes(int T, int d, int dff, int E, int k);
 int moe_forward_w8_ws(const void* x, const void* Wg, const int8_t* W1q, const float* W1s, const int8_t* W3q,

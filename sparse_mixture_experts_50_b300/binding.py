@@ -35,6 +35,7 @@ SIGNATURES = {
     "moe_router_topk": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _P]),
     "moe_rmsnorm": (_I, [_P, _P, _F, _P, _I, _I, _I, _P]),
     "moe_permute": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P]),
+    "moe_gather_rows": (_I, [_P, _I, _P, _I, _P, _SZ, _P]),
     "moe_expert_gate_up": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_expert_down": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -171,6 +172,18 @@ def moe_permute(x, topk_idx, E, out=None, stream=None):
     return counts, offsets, row_src, slot_pos, x_perm
 
 
+def moe_gather_rows(src, row_idx, dst=None, stream=None):
+    """dst[i] = src[row_idx[i]] (rows of any dtype, 16-byte multiples; row_idx int32)."""
+    _dev(src, row_idx, dst)
+    n = row_idx.shape[0]
+    if dst is None:
+        dst = src.new_empty((n,) + tuple(src.shape[1:]))
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else dst[0].numel() * dst.element_size()
+    _check("moe_gather_rows", lib().moe_gather_rows(_p(src), src.shape[0], _p(row_idx), n, _p(dst), row_bytes,
+                                                    _stream(stream)))
+    return dst
+
+
 def moe_expert_gate_up(x_perm, offsets, W1, W3, h_perm=None, stream=None):
     """Grouped gate/up GEMM + SwiGLU (step a4): returns h_perm[Tk,dff]."""
     _dev(x_perm, offsets, W1, W3, h_perm)
@@ -267,7 +280,7 @@ def workspace(T, d, dff, E, k, dtype=MOE_DTYPE_BF16, device="cuda", host=False):
 
 def w8_workspace(T, d, dff, E, k, device="cuda"):
     """Scratch for the int8 layer (moe_forward_w8_ws, moe_forward_ex with int8
-    weights) that lets large batches widen the codes once per call."""
+    weights): moe_forward_w8_workspace_bytes, the bf16 layer's size."""
     n = int(lib().moe_forward_w8_workspace_bytes(T, d, dff, E, k))
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 

@@ -135,21 +135,6 @@ struct W8Weights {
   const float* s2;
 };
 
-// The int8 layer at large batch widens the codes of all three matrices once
-// per call into bf16 scratch (3*E*dff*d*2 bytes after the layer's scratch)
-// and runs the bf16 GEMMs on them with the scales in the epilogue: that is
-// faster than widening every weight tile again for every row tile once the
-// experts average this many routed rows.
-constexpr long long kW8WidenRowsPerExpert = 512;
-
-bool w8_widen_pays(int T, int k, int E) {
-  return static_cast<long long>(T) * k >= kW8WidenRowsPerExpert * E;
-}
-
-size_t w8_widen_bytes(int d, int dff, int E) {
-  return 3 * ((static_cast<size_t>(E) * dff * d * 2 + 255) & ~static_cast<size_t>(255));
-}
-
 struct WsLayout {
   size_t idx, w, counts, offs, row_src, slot_pos, x_perm, h, y, xn, total;
 };
@@ -216,19 +201,7 @@ int forward_impl(const void* x, const void* gamma, float eps, const void* Wg, co
   MOE_TRY(launch_rc(launch_dispatch(idx, Tk, E, k, counts, offs, row_src, slot_pos, c, s)));
   MOE_TRY(launch_rc(launch_gather_rows(xin, row_src, x_perm, T, Tk, static_cast<size_t>(d) * esize(dtype), c, s)));
   MOE_TRY(mark(1));
-  if (w8 != nullptr && w8_widen_pays(T, k, E) && ws_bytes >= L.total + w8_widen_bytes(d, dff, E)) {
-    const size_t nw = static_cast<size_t>(E) * dff * d;
-    const size_t part = w8_widen_bytes(d, dff, E) / 3;
-    uint8_t* c1 = base + L.total;
-    uint8_t* c3 = c1 + part;
-    uint8_t* c2 = c3 + part;
-    MOE_TRY(launch_rc(launch_widen_int8(w8->q1, c1, nw, c, s)));
-    MOE_TRY(launch_rc(launch_widen_int8(w8->q3, c3, nw, c, s)));
-    MOE_TRY(launch_rc(launch_widen_int8(w8->q2, c2, nw, c, s)));
-    MOE_TRY(launch_tc_gate_up_scaled(x_perm, offs, c1, w8->s1, c3, w8->s3, h, Tk, d, dff, E, c, s));
-    MOE_TRY(mark(2));
-    MOE_TRY(launch_tc_down_scaled(h, offs, c2, w8->s2, y, Tk, d, dff, E, c, s));
-  } else if (w8 != nullptr) {
+  if (w8 != nullptr) {
     MOE_TRY(launch_w8_gate_up(x_perm, offs, w8->q1, w8->s1, w8->q3, w8->s3, h, Tk, d, dff, E, c, s));
     MOE_TRY(mark(2));
     MOE_TRY(launch_w8_down(h, offs, w8->q2, w8->s2, y, Tk, d, dff, E, c, s));
@@ -471,6 +444,19 @@ int moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int
   return launch_rc(launch_gather_rows(x, row_src, x_perm, T, Tk, static_cast<size_t>(d) * esize(dtype), c, stream));
 }
 
+int moe_gather_rows(const void* src, int src_rows, const int32_t* row_idx, int n_rows, void* dst, size_t row_bytes,
+                    moe_stream_t stream) {
+  if (src_rows < 0 || n_rows < 0) return MOE_EINVAL;
+  if (row_bytes == 0 || row_bytes % 16 != 0 || row_bytes / 16 > INT_MAX) return MOE_EINVAL;
+  if (n_rows == 0) return MOE_OK;
+  if (!src || !row_idx || !dst || !aligned(src, 16) || !aligned(dst, 16) || !aligned(row_idx, 4)) return MOE_EINVAL;
+  if (static_cast<long long>(n_rows) * static_cast<long long>(row_bytes / 16) > (1LL << 40)) return MOE_EUNSUPPORTED;
+  CtxScope scope;
+  MOE_TRY(scope.init(dst));
+  const Ctx& c = scope.ctx();
+  return launch_rc(launch_gather_rows(src, row_idx, dst, src_rows, n_rows, row_bytes, c, stream));
+}
+
 int moe_expert_gate_up(const void* x_perm, const int32_t* offsets, const void* W1, const void* W3, void* h_perm,
                        int Tk, int d, int dff, int E, int dtype, moe_stream_t stream) {
   MOE_TRY(check_ffn(Tk, d, dff, E, dtype));
@@ -554,8 +540,7 @@ size_t moe_workspace_bytes(int T, int d, int dff, int E, int k, int dtype) {
 
 size_t moe_forward_w8_workspace_bytes(int T, int d, int dff, int E, int k) {
   if (check_tokens(T, d, E, k, MOE_DTYPE_BF16) != MOE_OK || dff <= 0) return 0;
-  const size_t base = ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16).total;
-  return w8_widen_pays(T, k, E) ? base + w8_widen_bytes(d, dff, E) : base;
+  return ws_layout(T, d, dff, E, k, MOE_DTYPE_BF16).total;
 }
 
 int moe_forward_ws(const void* x, const void* Wg, const void* W1, const void* W3, const void* W2, void* out, int T,

@@ -138,15 +138,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // once instead of one row's latency after another.
 
 // The warp's 32 rows x 32 fp32 columns (lane = row, v[i] = column i) to
-// dst[r * ld + i] for r < rows: one coalesced 128-byte row per instruction.
+// dst[r * ld + i] for r < rows.  Each lane writes its row into the staging
+// block as eight 16-byte units (unit j of row r at unit j ^ (r & 7), so the
+// eight lanes of a quarter-warp meet distinct banks); then every load/store
+// instruction moves four whole 128-byte rows, a quarter-warp per row.
 __device__ __forceinline__ void warp_store_f32(uint32_t* stg, const uint32_t (&v)[32], float* dst, size_t ld,
                                                int rows, int lane) {
+  const uint32_t base = ptx::smem_u32(stg);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) stg[lane * STG_PITCH + i] = v[i];
+  for (int j = 0; j < 8; ++j)
+    ptx::sts128(base + lane * 128 + ((j ^ (lane & 7)) << 4),
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
   __syncwarp();
+  const int sub = lane >> 3, u = lane & 7;
 #pragma unroll
-  for (int r = 0; r < 32; ++r)
-    if (r < rows) dst[r * ld + lane] = __uint_as_float(stg[r * STG_PITCH + lane]);
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + sub;
+    const uint4 val = ptx::lds128(base + r * 128 + ((u ^ (r & 7)) << 4));
+    if (r < rows) *reinterpret_cast<uint4*>(dst + r * ld + 4 * u) = val;
+  }
   __syncwarp();
 }
 
@@ -176,17 +186,24 @@ __device__ __forceinline__ void swiglu_grad(float g, float a, float b, float& da
 }
 
 // The warp's 32 rows x 32 bf16 columns (lane = row, pk[i] = columns 2i,
-// 2i+1) to dst[r * ld + ...] for r < rows: two 64-byte rows per instruction.
+// 2i+1) to dst[r * ld + ...] for r < rows.  Each lane writes its 64-byte row
+// as four 16-byte units (unit j of row r at unit j ^ ((r >> 1) & 3), so a
+// quarter-warp meets distinct banks); then every load/store instruction moves
+// eight whole rows, four lanes per row.
 __device__ __forceinline__ void warp_store_bf16(uint32_t* stg, const uint32_t (&pk)[16], __nv_bfloat16* dst,
                                                 size_t ld, int rows, int lane) {
+  const uint32_t base = ptx::smem_u32(stg);
+  const int sw = (lane >> 1) & 3;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) stg[lane * 17 + i] = pk[i];
+  for (int j = 0; j < 4; ++j)
+    ptx::sts128(base + lane * 64 + ((j ^ sw) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
   __syncwarp();
-  const int half = lane >> 4, w = lane & 15;
+  const int sub = lane >> 2, u = lane & 3;
 #pragma unroll
-  for (int r2 = 0; r2 < 32; r2 += 2) {
-    const int r = r2 + half;
-    if (r < rows) reinterpret_cast<uint32_t*>(dst + r * ld)[w] = stg[r * 17 + w];
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + sub;
+    const uint4 val = ptx::lds128(base + r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+    if (r < rows) *reinterpret_cast<uint4*>(dst + r * ld + 8 * u) = val;
   }
   __syncwarp();
 }

@@ -21,20 +21,10 @@
 // offsets[E+1]; the host never reads the per-expert counts.
 //
 // int8 weights (KerasFormers Mixtral docs, "Lower memory": weight-only int8,
-// one fp32 scale per output row).  The weights stream from HBM as int8, half
-// the bytes of bf16, so the same kernel runs with:
-//   warp 0      TMA producer: per stage the bf16 A tile and the two raw int8
-//               B boxes (16 + 16 KB) into a 5-stage ring, so A is requested
-//               as early as the weights it meets;
-//   warps 6-9   converters: each widens its share of a stage's raw B to bf16
-//               (exact: every code in [-127, 127] is a bf16 value) and writes
-//               it into a 2-stage ring in the 128-byte-swizzled K-major
-//               layout tcgen05 reads;
-//   warp 1      MMA on A from the raw ring and B from the converted ring; a
-//               raw stage is free once the MMA and all converters are done;
-//   epilogue    multiplies each accumulator column by its row scale s[e, n]
-//               before the SwiGLU (gate/up) or the rounding (down): the scale
-//               of an output row factors out of its dot product.
+// one fp32 scale per output row) run here in the small-batch form below;
+// more rows go to ffn_w8_wide.cu.  The epilogue multiplies each accumulator
+// row by its scale s[e, n] before the SwiGLU (gate/up) or the rounding
+// (down): the scale of an output row factors out of its dot product.
 //
 // Small batches (decode).  With a few tokens per expert a 128-row token tile
 // is mostly padding, and the per-stage token tile costs as much shared
@@ -48,6 +38,9 @@
 // memory (tcgen05.st, one row per lane, two bf16 per column) and the MMA
 // takes its A operand from there: the widened weights never touch shared
 // memory, whose bandwidth would otherwise bound the small-batch int8 GEMM.
+// The converters are two groups of four warps taking alternate K steps: a
+// group's step is a chain of shared-memory loads, widening, tensor-memory
+// stores and their wait, and two groups overlap those chains.
 //
 // Every wait is bounded (globaltimer + iteration cap).  A wait that runs out
 // raises a CTA-wide abort flag and records MOE_ETIMEOUT; each role then
@@ -63,6 +56,7 @@
 
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "widen.cuh"
 
 namespace moe {
 namespace {
@@ -75,23 +69,11 @@ constexpr int BN = 2 * BN_HALF;          // MMA N
 constexpr int UMMA_K = 16;               // K of one tcgen05.mma (bf16)
 constexpr int B_HALF_BYTES = BN_HALF * BK * 2;
 constexpr int EPI_THREADS = 128;
-#ifndef MOE_W8_CONV_WARPS
-#define MOE_W8_CONV_WARPS 4
-#endif
-#ifndef MOE_W8_STAGES
-#define MOE_W8_STAGES 5
-#endif
-#ifndef MOE_W8_CONV_STAGES
-#define MOE_W8_CONV_STAGES 2
-#endif
 #ifndef MOE_SWAP_STAGES
 #define MOE_SWAP_STAGES 6
 #endif
 #ifndef MOE_W8_SWAP_STAGES
 #define MOE_W8_SWAP_STAGES 6
-#endif
-#ifndef MOE_CVT_F32X2
-#define MOE_CVT_F32X2 1
 #endif
 #ifndef MOE_TOK_STAGES
 #define MOE_TOK_STAGES 3
@@ -102,12 +84,9 @@ constexpr int EPI_THREADS = 128;
 #ifndef MOE_SWAP_MAX_ROWS
 #define MOE_SWAP_MAX_ROWS 128
 #endif
-constexpr int CONV_WARPS = MOE_W8_CONV_WARPS;  // int8 path: converter warps from warp 6
-constexpr int RAW_HALF_BYTES = BN_HALF * BK;          // one 128x64 int8 box, 8 KB
-constexpr int RAW_BYTES = 2 * RAW_HALF_BYTES;         // 16 KB per raw stage
+constexpr int CONV_WARPS = 4;     // int8: converter warps per group, one per tensor-memory lane quarter
+constexpr int CONV_GROUPS = 2;    // int8: converter groups, taking alternate K steps
 constexpr int MAX_STAGES = 10;
-constexpr int CONV_STAGES = MOE_W8_CONV_STAGES;  // int8 path: converted B stages (32 KB each)
-constexpr int CONV_BYTES = 2 * B_HALF_BYTES;
 // int8 small-batch mode: a stage covers 128 K of each weight row (128-byte
 // rows in every TMA request); its widened weights sit in tensor memory as two
 // 128-row halves x 128 K = 2 x 64 columns, after the 128 accumulator columns.
@@ -117,7 +96,6 @@ constexpr int TMEM_A_STAGES = MOE_TMEM_A_STAGES;
 constexpr int TMEM_A_COL0 = 128;
 constexpr int TMEM_A_HALF_COLS = BK_W / 2;
 constexpr int TMEM_A_STAGE_COLS = 2 * TMEM_A_HALF_COLS;
-constexpr int RING_MAX = CONV_STAGES > TMEM_A_STAGES ? CONV_STAGES : TMEM_A_STAGES;
 constexpr int MAX_E = 64;
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 constexpr uint32_t IDESC_SWAP = ptx::idesc_bf16_f32(BN_HALF, TN);
@@ -127,8 +105,8 @@ constexpr int SWAP_MAX_ROWS = MOE_SWAP_MAX_ROWS;
 struct SmemCtl {
   uint64_t full[MAX_STAGES];       // a stage's TMA copies landed
   uint64_t empty[MAX_STAGES];      // the MMA (and, int8 path, every converter) is done with a stage
-  uint64_t c_full[RING_MAX];       // int8 path: widened weights written (shared or tensor memory)
-  uint64_t c_empty[RING_MAX];      // int8 path: the MMA is done with widened weights
+  uint64_t c_full[TMEM_A_STAGES];  // int8: widened weights written to tensor memory
+  uint64_t c_empty[TMEM_A_STAGES]; // int8: the MMA is done with them
   uint64_t tok_full[8];            // int8 small-batch mode: token tile landed
   uint64_t tok_empty[8];           // int8 small-batch mode: the MMA is done with a token tile
   uint64_t tfull[2];
@@ -142,37 +120,33 @@ struct SmemCtl {
 };
 
 // Plan of each mode.  A shared-memory stage is the token tile (128 rows, or
-// 32 when swapped) + the weights (bf16, or raw int8).  bf16: 4 stages (6
-// swapped).  int8: 5 stages + 2 stages of widened weights in shared memory.
-// int8 swapped: the weights no longer wait for the MMA (it reads them from
+// 32 when swapped) + the bf16 weights: 4 stages (6 swapped).  int8 (always
+// swapped): the weights no longer wait for the MMA (it reads them from
 // tensor memory), so they get a ring of their own, 6 stages of 256 rows x
 // 128 K, freed by the converters; the token tiles have a 3-stage ring with
 // a producer warp of their own, freed by the MMA; 3 stages of widened
 // weights in tensor memory.
 template <bool W8, bool SWAP>
 struct Plan {
-  static constexpr bool tmem_a = W8 && SWAP;             // A operand (widened weights) in tensor memory
+  static_assert(!W8 || SWAP, "int8 weights: small-batch form only");
+  static constexpr bool tmem_a = W8;                     // A operand (widened weights) in tensor memory
   static constexpr int kstep = tmem_a ? BK_W : BK;       // K per stage
   static constexpr int rows = SWAP ? TN : BM;            // token rows per tile
   static constexpr int tok_box_bytes = rows * BK * 2;    // one 64-wide token box
   static constexpr int a_bytes = (kstep / BK) * tok_box_bytes;  // token tile per stage
-  static constexpr int raw_half_bytes = tmem_a ? RAW_W_HALF_BYTES : RAW_HALF_BYTES;
   static constexpr int b_off = tmem_a ? 0 : a_bytes;     // weights' offset in a stage
-  static constexpr int stage_bytes = b_off + (W8 ? 2 * raw_half_bytes : 2 * B_HALF_BYTES);
+  static constexpr int stage_bytes = b_off + (W8 ? 2 * RAW_W_HALF_BYTES : 2 * B_HALF_BYTES);
   static constexpr int tok_stages = tmem_a ? MOE_TOK_STAGES : 0;  // separate token ring
-  static constexpr int tok_warp = 6 + CONV_WARPS;        // its producer (int8 swapped)
-  static constexpr int stages = SWAP ? (W8 ? MOE_W8_SWAP_STAGES : MOE_SWAP_STAGES) : (W8 ? MOE_W8_STAGES : 4);
-  static constexpr int conv_stages = (W8 && !SWAP) ? CONV_STAGES : 0;  // shared-memory widened stages
-  static constexpr int wide_stages = tmem_a ? TMEM_A_STAGES : CONV_STAGES;
-  static constexpr int threads = W8 ? 192 + 32 * CONV_WARPS + (tmem_a ? 32 : 0) : 192;
+  static constexpr int conv_warps = W8 ? CONV_WARPS * CONV_GROUPS : 0;  // from warp 6
+  static constexpr int tok_warp = 6 + conv_warps;        // the token ring's producer (int8)
+  static constexpr int stages = SWAP ? (W8 ? MOE_W8_SWAP_STAGES : MOE_SWAP_STAGES) : 4;
+  static constexpr int threads = 192 + 32 * conv_warps + (tmem_a ? 32 : 0);
   static constexpr int acc_cols = SWAP ? 2 * TN : BN;    // fp32 columns of one accumulator
   static constexpr int tmem_cols = (SWAP && !W8) ? 128 : 512;  // power of two
   static_assert(!tmem_a || TMEM_A_COL0 + TMEM_A_STAGES * TMEM_A_STAGE_COLS <= 512, "tensor-memory ring too deep");
   static_assert(!tmem_a || 2 * acc_cols <= TMEM_A_COL0, "accumulators overlap the widened weights");
-  static_assert(!tmem_a || CONV_WARPS == 4 || CONV_WARPS == 8, "converter warps per tensor-memory lane quarter: 1 or 2");
   static_assert(tok_stages <= 8, "token ring too deep");
   static constexpr size_t ring_bytes = static_cast<size_t>(stages) * stage_bytes +
-                                       static_cast<size_t>(conv_stages) * CONV_BYTES +
                                        static_cast<size_t>(tok_stages) * a_bytes;
   static constexpr size_t smem_bytes = 1024 + ring_bytes + sizeof(SmemCtl);
   static_assert(stages <= MAX_STAGES, "too many stages");
@@ -227,36 +201,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Four int8 codes (one 32-bit word, element 0 in the low byte) -> four bf16
-// (two words), exactly.  Flipping the sign bit gives b + 128 in [0, 255] as an
-// unsigned byte; placed in the low mantissa bits of the fp32 2^23 it is the
-// fp32 value 2^23 + b + 128, and subtracting 2^23 + 128 leaves b exactly.  A
-// value of at most 8 significant bits has zero low 16 bits in fp32, so its
-// bf16 encoding is the high half of the fp32 word.
-__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-#if MOE_CVT_F32X2
-  // The two subtractions of a pair as one packed fp32x2 add of -(2^23 + 128).
-  constexpr unsigned long long kBias2 = 0xCB000080CB000080ull;
-  unsigned long long p01 = (static_cast<unsigned long long>(__byte_perm(u, 0x4B000000u, 0x7541)) << 32) |
-                           __byte_perm(u, 0x4B000000u, 0x7540);
-  unsigned long long p23 = (static_cast<unsigned long long>(__byte_perm(u, 0x4B000000u, 0x7543)) << 32) |
-                           __byte_perm(u, 0x4B000000u, 0x7542);
-  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p01) : "l"(kBias2));
-  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p23) : "l"(kBias2));
-  lo = __byte_perm(static_cast<uint32_t>(p01), static_cast<uint32_t>(p01 >> 32), 0x7632);
-  hi = __byte_perm(static_cast<uint32_t>(p23), static_cast<uint32_t>(p23 >> 32), 0x7632);
-#else
-  constexpr float kBias = 8388736.0f;  // 2^23 + 128
-  const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - kBias;
-  const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - kBias;
-  const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - kBias;
-  const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - kBias;
-  lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-  hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
-#endif
-}
-
 // What the training forward keeps for the backward of h = silu(a) b, formed
 // in fp32 from the GEMM's fp32 a and b and rounded once to bf16:
 // p = dh/da / dh = b silu'(a) = b s (1 + a (1 - s)) and q = dh/db / dh =
@@ -280,8 +224,7 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
   constexpr int ROWS = P::rows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* conv = smem + NST * SB;  // int8 path: converted B stages
-  uint8_t* toks = smem + NST * SB;  // int8 swapped: token ring (no converted stages then)
+  uint8_t* toks = smem + NST * SB;  // int8: token ring
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + P::ring_bytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -292,13 +235,13 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
-      ptx::mbar_init(&ctl->empty[s], W8 ? (P::tmem_a ? 0 : 1) + CONV_WARPS : 1);
+      ptx::mbar_init(&ctl->empty[s], W8 ? CONV_WARPS : 1);
     }
     for (int s = 0; s < P::tok_stages; ++s) {
       ptx::mbar_init(&ctl->tok_full[s], 1);
       ptx::mbar_init(&ctl->tok_empty[s], 1);
     }
-    for (int s = 0; s < (W8 ? P::wide_stages : 0); ++s) {
+    for (int s = 0; s < (W8 ? TMEM_A_STAGES : 0); ++s) {
       ptx::mbar_init(&ctl->c_full[s], CONV_WARPS);
       ptx::mbar_init(&ctl->c_empty[s], 1);
     }
@@ -379,7 +322,7 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
             break;
           }
           uint8_t* sa = smem + stage * SB;
-          constexpr int half = W8 ? P::raw_half_bytes : B_HALF_BYTES;
+          constexpr int half = W8 ? RAW_W_HALF_BYTES : B_HALF_BYTES;
           const int k0 = kb * P::kstep;
           ptx::mbar_arrive_expect_tx(&ctl->full[stage], SB);
           if (!P::tmem_a) {
@@ -429,7 +372,7 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t sa = P::tmem_a ? ptx::smem_u32(toks + stage * AB) : ptx::smem_u32(smem + stage * SB);
-          const uint32_t sb = (W8 && !SWAP) ? ptx::smem_u32(conv + cstage * CONV_BYTES) : sa + AB;
+          const uint32_t sb = sa + AB;
           const uint32_t ta = tmem_base + TMEM_A_COL0 + static_cast<uint32_t>(cstage * TMEM_A_STAGE_COLS);
 #pragma unroll
           for (int kk = 0; kk < P::kstep / UMMA_K; ++kk) {
@@ -457,7 +400,7 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
           ptx::umma_commit(P::tmem_a ? &ctl->tok_empty[stage] : &ctl->empty[stage]);
           if (W8) {
             ptx::umma_commit(&ctl->c_empty[cstage]);
-            if (++cstage == P::wide_stages) {
+            if (++cstage == TMEM_A_STAGES) {
               cstage = 0;
               cphase ^= 1u;
             }
@@ -657,16 +600,27 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
       }
     }
   } else if (W8) {
-    // -------------------------------------------------- converters (warps 6-9, int8 path)
-    // Per stage: wait until the MMA is done with the converted stage and the
-    // raw stage has landed, widen the raw B to bf16 into the swizzled layout,
-    // then mark the converted stage ready and release the raw stage.
-    const int ct = threadIdx.x - 192;  // 0 .. 32 * CONV_WARPS - 1
-    int stage = 0, cstage = 0;
-    uint32_t phase = 0, cphase = 0;
+    // -------------------------------------------------- converters (int8, warps 6-13)
+    // Warp q (= warp % 4) may access tensor-memory lanes 32q .. 32q+31: lane
+    // r holds weight row r of each 128-row half, 128 K values as 64 columns.
+    // The raw tile was stored with the 128-byte swizzle (16-byte unit u of
+    // row r at unit u ^ (r % 8)), so the row reads of 8 lanes hit distinct
+    // banks.  Group g takes the K steps c (counted over all of the CTA's
+    // tiles) with c % CONV_GROUPS == g.  Per step: wait until the MMA is
+    // done with the tensor-memory stage and the raw stage has landed, widen,
+    // store, then mark the widened stage ready and release the raw stage.
+    const uint32_t grp = static_cast<uint32_t>(warp - 6) / CONV_WARPS;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + TMEM_A_COL0;
+    uint32_t cnt = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = 0; kb < kblocks; ++kb, ++cnt) {
+        if (cnt % CONV_GROUPS != grp) continue;
+        const int stage = static_cast<int>(cnt % NST);
+        const uint32_t phase = (cnt / NST) & 1u;
+        const int cstage = static_cast<int>(cnt % TMEM_A_STAGES);
+        const uint32_t cphase = (cnt / TMEM_A_STAGES) & 1u;
         // Waits are warp-uniform: the warp goes on or leaves as one.
         const bool ready = ptx::mbar_wait(&ctl->c_empty[cstage], cphase ^ 1u, abort_flag, args.wait_ns) &&
                            ptx::mbar_wait(&ctl->full[stage], phase, abort_flag, args.wait_ns);
@@ -675,95 +629,33 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
           ok = false;
           break;
         }
-        if (P::tmem_a) {
-          // Warp q (= warp % 4) may access tensor-memory lanes 32q .. 32q+31:
-          // lane r holds weight row r of a 128-row half, 128 K values as 64
-          // columns.  With 4 converter warps each does both halves; with 8,
-          // warps 6-9 do half 0 and warps 10-13 half 1.  The raw tile was
-          // stored with the 128-byte swizzle (16-byte unit u of row r at unit
-          // u ^ (r % 8)), so the row reads of 8 lanes hit distinct banks.
-          const int r = (warp & 3) * 32 + lane;
-          const uint32_t rs = ptx::smem_u32(smem + stage * SB + P::b_off) + r * BK_W;
-          const uint32_t tl = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + TMEM_A_COL0 +
-                              static_cast<uint32_t>(cstage * TMEM_A_STAGE_COLS);
-          constexpr int kHalves = CONV_WARPS == 8 ? 1 : 2;
-          const int hf0 = CONV_WARPS == 8 ? (warp - 6) / 4 : 0;
+        const uint32_t rs = ptx::smem_u32(smem + stage * SB) + r * BK_W;
+        const uint32_t tl = t_lane + static_cast<uint32_t>(cstage * TMEM_A_STAGE_COLS);
 #pragma unroll
-          for (int hi = 0; hi < kHalves; ++hi) {
-            const int hf = hf0 + hi;
+        for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {  // 64 codes = 32 columns at a time
-              uint4 v[4];
+          for (int q = 0; q < 2; ++q) {  // 64 codes = 32 columns at a time
+            uint4 v[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                v[u] = ptx::lds128(rs + hf * RAW_W_HALF_BYTES + (((4 * q + u) ^ (r & 7)) << 4));
-              uint32_t w[32];
+            for (int u = 0; u < 4; ++u)
+              v[u] = ptx::lds128(rs + hf * RAW_W_HALF_BYTES + (((4 * q + u) ^ (r & 7)) << 4));
+            uint32_t w[32];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                i8x4_to_bf16x4(v[u].x, w[8 * u + 0], w[8 * u + 1]);
-                i8x4_to_bf16x4(v[u].y, w[8 * u + 2], w[8 * u + 3]);
-                i8x4_to_bf16x4(v[u].z, w[8 * u + 4], w[8 * u + 5]);
-                i8x4_to_bf16x4(v[u].w, w[8 * u + 6], w[8 * u + 7]);
-              }
-              ptx::tmem_st_32x32b_x32(tl + hf * TMEM_A_HALF_COLS + q * 32, w);
+            for (int u = 0; u < 4; ++u) {
+              i8x4_to_bf16x4(v[u].x, w[8 * u + 0], w[8 * u + 1]);
+              i8x4_to_bf16x4(v[u].y, w[8 * u + 2], w[8 * u + 3]);
+              i8x4_to_bf16x4(v[u].z, w[8 * u + 4], w[8 * u + 5]);
+              i8x4_to_bf16x4(v[u].w, w[8 * u + 6], w[8 * u + 7]);
             }
+            ptx::tmem_st_32x32b_x32(tl + hf * TMEM_A_HALF_COLS + q * 32, w);
           }
-          ptx::tmem_st_wait();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive(&ctl->c_full[cstage]);
-            ptx::mbar_arrive(&ctl->empty[stage]);
-          }
-          if (++cstage == P::wide_stages) {
-            cstage = 0;
-            cphase ^= 1u;
-          }
-          if (++stage == NST) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          continue;
         }
-        // 1024 chunks of 16 codes: chunk ci is row ci/4 (of 256: B0 rows
-        // 0-127 then B1 rows), codes 16*(ci%4) .. +15 of the stage's 64.  A
-        // warp reads 512 consecutive bytes; its 16-byte stores land on
-        // distinct banks under the 128-byte swizzle (unit j of row r is
-        // stored at unit j ^ (r % 8)).
-        const uint32_t rs = ptx::smem_u32(smem + stage * SB + AB);
-        const uint32_t sb = ptx::smem_u32(conv + cstage * CONV_BYTES);
-        constexpr int kChunks = (RAW_BYTES / 16) / (32 * CONV_WARPS);
-        uint4 v[kChunks];
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) v[i] = ptx::lds128(rs + (i * (32 * CONV_WARPS) + ct) * 16);
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-          const int ci = i * (32 * CONV_WARPS) + ct;
-          const int r = ci >> 2;
-          const int kc = ci & 3;
-          uint4 lo, hi;
-          i8x4_to_bf16x4(v[i].x, lo.x, lo.y);
-          i8x4_to_bf16x4(v[i].y, lo.z, lo.w);
-          i8x4_to_bf16x4(v[i].z, hi.x, hi.y);
-          i8x4_to_bf16x4(v[i].w, hi.z, hi.w);
-          const uint32_t row = sb + r * 128;
-          const int sw = r & 7;
-          ptx::sts128(row + (((2 * kc) ^ sw) << 4), lo);
-          ptx::sts128(row + (((2 * kc + 1) ^ sw) << 4), hi);
-        }
-        ptx::fence_proxy_async_smem();  // the MMA reads these through the async proxy
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           ptx::mbar_arrive(&ctl->c_full[cstage]);
           ptx::mbar_arrive(&ctl->empty[stage]);
-        }
-        if (++cstage == P::wide_stages) {
-          cstage = 0;
-          cphase ^= 1u;
-        }
-        if (++stage == NST) {
-          stage = 0;
-          phase ^= 1u;
         }
       }
     }
@@ -909,9 +801,14 @@ int launch_gemm(const void* A, const void* B0, const void* B1, const float* S0, 
   a.n_tiles = SWIGLU ? (n_out + BN_HALF - 1) / BN_HALF : (n_out + BN - 1) / BN;
   a.status = c.status;
   a.wait_ns = c.wait_ns;
-  // Few rows (decode): weights as the MMA's M operand, 32 tokens as N.
-  if (Tk <= SWAP_MAX_ROWS) return launch_mode<SWIGLU, W8, true>(A, B0, B1, a, c, s);
-  return launch_mode<SWIGLU, W8, false>(A, B0, B1, a, c, s);
+  // Few rows (decode): weights as the MMA's M operand, 32 tokens as N.  The
+  // int8 weights come here only with few rows (more go to the wide kernel).
+  if constexpr (W8) {
+    return launch_mode<SWIGLU, true, true>(A, B0, B1, a, c, s);
+  } else {
+    if (Tk <= SWAP_MAX_ROWS) return launch_mode<SWIGLU, false, true>(A, B0, B1, a, c, s);
+    return launch_mode<SWIGLU, false, false>(A, B0, B1, a, c, s);
+  }
 }
 
 }  // namespace
@@ -940,11 +837,13 @@ int launch_tc_down_scaled(const void* h, const int32_t* offsets, const void* W2c
 int launch_w8_gate_up(const void* x_perm, const int32_t* offsets, const int8_t* W1q, const float* W1s,
                       const int8_t* W3q, const float* W3s, void* h, int Tk, int d, int dff, int E, const Ctx& c,
                       cudaStream_t s) {
+  if (Tk > SWAP_MAX_ROWS) return launch_w8_wide_gate_up(x_perm, offsets, W1q, W1s, W3q, W3s, h, Tk, d, dff, E, c, s);
   return launch_gemm<true, true>(x_perm, W1q, W3q, W1s, W3s, offsets, h, Tk, d, dff, dff, E, c, s);
 }
 
 int launch_w8_down(const void* h, const int32_t* offsets, const int8_t* W2q, const float* W2s, void* y, int Tk, int d,
                    int dff, int E, const Ctx& c, cudaStream_t s) {
+  if (Tk > SWAP_MAX_ROWS) return launch_w8_wide_down(h, offsets, W2q, W2s, y, Tk, d, dff, E, c, s);
   return launch_gemm<false, true>(h, W2q, nullptr, W2s, nullptr, offsets, y, Tk, dff, d, d, E, c, s);
 }
 

@@ -146,17 +146,12 @@ def test_binding_refuses_cpu_tensors():
 
 
 def test_w8_workspace_bytes(lib):
-    """The int8 layer asks for the codes' widened copy (3*E*dff*d*2 bytes,
-    each matrix 256-byte aligned) exactly when the experts average at least
-    512 routed rows."""
+    """The int8 layer needs the bf16 layer's scratch and nothing more: its
+    weights are widened on the SM, never into a bf16 copy."""
     d, F, E, k = 4096, 14336, 8, 2
-    base = lambda T: lib.moe_workspace_bytes(T, d, F, E, k, B.MOE_DTYPE_BF16)
-    wide = 3 * ((E * F * d * 2 + 255) // 256 * 256)
-    assert lib.moe_forward_w8_workspace_bytes(16, d, F, E, k) == base(16)
-    assert lib.moe_forward_w8_workspace_bytes(4096, d, F, E, k) == base(4096) + wide
-    t0 = 512 * E // k                      # T*k == 512*E: the first T that widens
-    assert lib.moe_forward_w8_workspace_bytes(t0, d, F, E, k) == base(t0) + wide
-    assert lib.moe_forward_w8_workspace_bytes(t0 - 1, d, F, E, k) == base(t0 - 1)
+    for T in (1, 16, 2047, 2048, 4096, 8192):
+        assert lib.moe_forward_w8_workspace_bytes(T, d, F, E, k) == \
+            lib.moe_workspace_bytes(T, d, F, E, k, B.MOE_DTYPE_BF16)
     assert lib.moe_forward_w8_workspace_bytes(-1, d, F, E, k) == 0
 
 
@@ -180,3 +175,13 @@ def test_training_entry_validation(lib):
     assert call(saved_bytes=saved - 1) == B.MOE_ENOMEM  # saved scratch too small
     assert call(ws_bytes=need - 1) == B.MOE_ENOMEM      # backward scratch too small
     assert call(T=0) == B.MOE_OK
+
+
+def test_gather_rows_validation(lib):
+    f = lib.moe_gather_rows
+    assert f(FAKE, 10, FAKE, 4, FAKE, 24, NULL) == B.MOE_EINVAL       # row bytes not a multiple of 16
+    assert f(FAKE, 10, FAKE, 4, FAKE, 0, NULL) == B.MOE_EINVAL        # empty rows
+    assert f(FAKE + 8, 10, FAKE, 4, FAKE, 32, NULL) == B.MOE_EINVAL   # misaligned src
+    assert f(FAKE, 10, NULL, 4, FAKE, 32, NULL) == B.MOE_EINVAL       # null index
+    assert f(FAKE, -1, FAKE, 4, FAKE, 32, NULL) == B.MOE_EINVAL
+    assert f(NULL, 0, NULL, 0, NULL, 32, NULL) == B.MOE_OK            # nothing to copy
