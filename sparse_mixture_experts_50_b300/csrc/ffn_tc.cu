@@ -158,9 +158,7 @@ struct GemmArgs {
   const int32_t* offsets;  // [E+1], device
   __nv_bfloat16* out;      // [Tk, ldo]
   const float* scale0;     // int8 path: row scales of B0 [E * b_rows]
-  const float* scale1;     // int8 path: row scales of B1 (gate/up only); also set,
-                           // with bf16 B holding the widened int8 codes, for the
-                           // int8 layer at large batch (scaled in the epilogue)
+  const float* scale1;     // int8 path: row scales of B1 (gate/up only)
   __nv_bfloat16* keep;     // bf16 gate/up, optional (training): the SwiGLU's
                            // local derivatives, planes [2, Tk, ldo] (see keep_pair)
   int ldo;                 // row stride of out (elements)
@@ -425,7 +423,7 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
     // -------------------------------------------------- epilogue (warps 2-5)
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. +31
     const int row_in_tile = quad * 32 + lane;
-    const bool scaled = W8 || args.scale0 != nullptr;  // per-weight-row scales in the epilogue
+    constexpr bool scaled = W8;  // per-weight-row scales in the epilogue
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -821,17 +819,6 @@ int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1
 int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d, int dff, int E,
                    const Ctx& c, cudaStream_t s) {
   return launch_gemm<false, false>(h, W2, nullptr, nullptr, nullptr, offsets, y, Tk, dff, d, d, E, c, s);
-}
-
-int launch_tc_gate_up_scaled(const void* x_perm, const int32_t* offsets, const void* W1c, const float* W1s,
-                             const void* W3c, const float* W3s, void* h, int Tk, int d, int dff, int E, const Ctx& c,
-                             cudaStream_t s) {
-  return launch_gemm<true, false>(x_perm, W1c, W3c, W1s, W3s, offsets, h, Tk, d, dff, dff, E, c, s);
-}
-
-int launch_tc_down_scaled(const void* h, const int32_t* offsets, const void* W2c, const float* W2s, void* y, int Tk,
-                          int d, int dff, int E, const Ctx& c, cudaStream_t s) {
-  return launch_gemm<false, false>(h, W2c, nullptr, W2s, nullptr, offsets, y, Tk, dff, d, d, E, c, s);
 }
 
 int launch_w8_gate_up(const void* x_perm, const int32_t* offsets, const int8_t* W1q, const float* W1s,

@@ -111,15 +111,6 @@ int launch_tc_gate_up(const void* x_perm, const int32_t* offsets, const void* W1
                       void* h, int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s, void* keep = nullptr);
 int launch_tc_down(const void* h, const int32_t* offsets, const void* W2, void* y, int Tk, int d,
                    int dff, int E, const Ctx& c, cudaStream_t s);
-// The bf16 GEMMs on widened int8 codes (bf16 integers) with the per-row
-// scales applied in the epilogue: the int8 layer at large batch.
-int launch_tc_gate_up_scaled(const void* x_perm, const int32_t* offsets, const void* W1c, const float* W1s,
-                             const void* W3c, const float* W3s, void* h, int Tk, int d, int dff, int E, const Ctx& c,
-                             cudaStream_t s);
-int launch_tc_down_scaled(const void* h, const int32_t* offsets, const void* W2c, const float* W2s, void* y, int Tk,
-                          int d, int dff, int E, const Ctx& c, cudaStream_t s);
-// int8 codes -> bf16 (exact: |q| <= 127), n elements, n % 16 == 0.
-cudaError_t launch_widen_int8(const int8_t* q, void* out, size_t n, const Ctx& c, cudaStream_t s);
 // Backward (bf16 activations, fp32 weight gradients).
 int dwg_chunks(int T);
 // keep == NULL: dh (fp32) to `dh`; else the forward's p and q ([2, Tk, dff]

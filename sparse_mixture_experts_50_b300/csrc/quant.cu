@@ -20,12 +20,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Two int8 values as bf16 (low half = lo); exact, since |q| <= 127 needs 7 bits.
-__device__ __forceinline__ uint32_t pack_bf16x2_exact(int8_t lo, int8_t hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(lo), static_cast<float>(hi));
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 __device__ __forceinline__ void bf16x8(const __nv_bfloat16* p, float (&v)[8]) {
   const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -76,27 +70,6 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_int8_kernel(const __nv
   }
 }
 
-// int8 codes -> bf16 codes (exact), 16 per thread and step: one 16-byte
-// load, two 16-byte stores.
-__global__ void __launch_bounds__(kThreads) widen_int8_kernel(const uint4* __restrict__ q, uint4* __restrict__ out,
-                                                             size_t n16) {
-  pdl_enter();
-  const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
-  for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; i < n16; i += stride) {
-    const uint4 v = __ldg(q + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int8_t* b = reinterpret_cast<const int8_t*>(&w[j]);
-      o[2 * j] = pack_bf16x2_exact(b[0], b[1]);
-      o[2 * j + 1] = pack_bf16x2_exact(b[2], b[3]);
-    }
-    out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
-    out[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_quantize_int8(const void* W, long long rows, int cols, int8_t* q, float* scale, const Ctx& c,
@@ -107,17 +80,6 @@ cudaError_t launch_quantize_int8(const void* W, long long rows, int cols, int8_t
   if (blocks < 1) blocks = 1;
   launch_pdl(quantize_rows_int8_kernel, static_cast<int>(blocks), kThreads, 0, s,
              static_cast<const __nv_bfloat16*>(W), rows, cols, q, scale);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_widen_int8(const int8_t* q, void* out, size_t n, const Ctx& c, cudaStream_t s) {
-  const size_t n16 = n / 16;
-  if (n16 == 0) return cudaSuccess;
-  size_t blocks = (n16 + kThreads - 1) / kThreads;
-  const size_t cap = static_cast<size_t>(c.num_sms) * 8;
-  if (blocks > cap) blocks = cap;
-  launch_pdl(widen_int8_kernel, static_cast<int>(blocks), kThreads, 0, s, reinterpret_cast<const uint4*>(q),
-             static_cast<uint4*>(out), n16);
   return cudaGetLastError();
 }
 
