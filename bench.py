@@ -93,7 +93,7 @@ def algorithmic(wl, counts):
 # ---------------------------------------------------------------- ncu traffic
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("ffn_tc.cu", "ptx.cuh"):
+    for name in ("ffn_tc.cu", "ffn_w8_wide.cu", "widen.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "sparse_mixture_experts_50_b300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
