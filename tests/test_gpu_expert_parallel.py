@@ -90,3 +90,46 @@ def test_expert_parallel_matches_layer(B, G, tokens):
         if not np.array_equal(idx_eff, ora_idx):
             ref = O.moe_forward_with_routing(xs_cpu[s], t["W1"], t["W3"], t["W2"], w_eff, idx_eff)
         check_close(to_np(outs[s]), ref, "bf16", f"rank {s} vs the oracle")
+
+
+def _nccl_rank(q):
+    import os
+    import sys
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(31500 + os.getpid() % 1000), RANK="0",
+                      WORLD_SIZE="1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    sys.path.insert(0, os.path.join(root, "tests"))
+    import torch
+    import torch.distributed as dist
+
+    import moe_workloads as mw
+    from sparse_mixture_experts_50_b300 import binding
+    from sparse_mixture_experts_50_b300.expert_parallel import ExpertParallelMoE, TorchComm
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda:0"))
+    try:
+        wl = mw.get("small_bf16")
+        g = {n: v.to("cuda:0") for n, v in mw.make_inputs(wl).items()}
+        layer = ExpertParallelMoE(g["Wg"], g["W1"], g["W3"], g["W2"], wl.k, TorchComm())
+        out = layer.forward(g["x"])
+        ref = binding.moe_forward(g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], wl.k)
+        torch.cuda.synchronize()
+        q.put((bool(torch.equal(out, ref)), binding.moe_get_device_status(reset=True)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_expert_parallel_forward_over_nccl_one_rank(B):
+    """ExpertParallelMoE.forward with TorchComm over NCCL (one rank, device
+    tensors): the exchange is the identity, so the output must equal
+    moe_forward's bit for bit."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_nccl_rank, args=(q,))
+    p.start()
+    p.join(timeout=300)
+    assert p.exitcode == 0
+    same, status = q.get(timeout=5)
+    assert status == 0 and same
