@@ -614,7 +614,7 @@ def main():
     peaks = load_peaks()
     shared = {}
     results = {}
-    head_layer = None
+    e2e = None
     for name in names:
         # SM clocks are sampled during every workload: the dense ones run at
         # the power cap, below the maximum clock.
@@ -622,12 +622,14 @@ def main():
         clocks.start()
         res, layer = bench_workload(name, shared, args, device, peaks, dist_on)
         res["clocks"] = clocks.stop()
+        if name == head_name and not args.no_e2e:
+            # Right after the headline's device-timed steps, before the
+            # oracle's accuracy pass (whose host threads would share the
+            # cores with this host-timed loop) and the other workloads.
+            e2e = e2e_leg(layer, args.steps, args.warmup)
         if rank == 0 and not args.no_cpu_baseline and not mw.get(name).bwd:
             res["accuracy"] = accuracy(layer, make_tensors(mw.get(name), shared))
-        if name == head_name:
-            head_layer = layer
-        else:
-            del layer
+        del layer
         results[name] = res
         torch.cuda.empty_cache()
 
@@ -636,7 +638,6 @@ def main():
     t_local = head["ms_per_step"] * args.steps * 1e-3
     value, _ = job_throughput(mw.get(head_name).T * args.steps, t_local, dist_on, device)
 
-    e2e = None if args.no_e2e else e2e_leg(head_layer, args.steps, args.warmup)
     if dist_on and e2e is not None:
         # every rank ran the same number of host-timed steps
         T = mw.get(head_name).T
