@@ -323,11 +323,23 @@ def bench_backward(name, shared, args, device, peaks, dist_on):
         "workload": name, "T": wl.T, "tokens_per_s": wl.T / (ms * 1e-3), "ms_per_step": ms,
         "ms_per_step_median": statistics.median(step_ms), "train_forward_ms": fwd,
         "layer_roofline_frac": achieved / peaks["bf16_tflops"], "bound": "tensor",
+        "layer_roofline_frac_of_nominal": of_nominal("tensor", achieved),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"],
+                     "frac": achieved / peaks["bf16_tflops"], "frac_of_nominal": of_nominal("tensor", achieved),
                      "kernel": "whole backward (moe_backward_ws)", "algorithmic_per_launch": flops, "traffic": None},
         "wall_s": wall,
     }, layer
+
+
+# Nominal B300 figures, reported beside the fractions of the measured peaks:
+# HBM3e ~8 TB/s and dense bf16 2.25 PFLOP/s.
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
+
+
+def of_nominal(bound, achieved):
+    """achieved (GB/s for an HBM-bound kernel, TFLOP/s for a tensor-bound
+    one) as a fraction of the nominal peak."""
+    return achieved / (NOMINAL["hbm_gbs"] if bound == "hbm" else NOMINAL["bf16_tflops"])
 
 
 def bench_workload(name, shared, args, device, peaks, dist_on):
@@ -348,6 +360,7 @@ def bench_workload(name, shared, args, device, peaks, dist_on):
     ms = sum(step_ms) / len(step_ms)
     flops, nbytes, gu_flops, gu_bytes = algorithmic(wl, counts)
     t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    t_nominal = max(flops / (NOMINAL["bf16_tflops"] * 1e12), nbytes / (NOMINAL["hbm_gbs"] * 1e9))
     bound = "hbm" if nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (peaks["bf16_tflops"] * 1e12) else "tensor"
     gu_ms = sum(parts["gate_up"]) / len(parts["gate_up"])
     if bound == "hbm":
@@ -358,10 +371,12 @@ def bench_workload(name, shared, args, device, peaks, dist_on):
         "workload": name, "T": wl.T, "tokens_per_s": wl.T / (ms * 1e-3), "ms_per_step": ms,
         "ms_per_step_median": statistics.median(step_ms),
         "layer_roofline_frac": t_roof / (ms * 1e-3), "bound": bound,
+        "layer_roofline_frac_of_nominal": t_nominal / (ms * 1e-3),
         "layer_roofline_tokens_per_s": wl.T / t_roof,
         "kernel_ms": {p: sum(v) / len(v) for p, v in parts.items()},
         "expert_counts": counts,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "frac_of_nominal": of_nominal(bound, achieved),
                      "kernel": "grouped_gemm_tc_kernel<gate_up+SwiGLU%s>" % (", int8 weights" if wl.w8 else ""),
                      "algorithmic_per_launch": gu_bytes if bound == "hbm" else gu_flops,
                      "traffic": ncu_traffic(name)},
@@ -654,7 +669,9 @@ def main():
             "config": config_of(head_name, world), "impl": "native",
             "roofline": {k: head["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
             "roofline_detail": {**head["roofline"], "peak_source": peaks["source"],
-                                "layer_frac": head["layer_roofline_frac"]},
+                                "layer_frac": head["layer_roofline_frac"],
+                                "layer_frac_of_nominal": head["layer_roofline_frac_of_nominal"],
+                                "nominal_peaks": NOMINAL},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": KERNELS_PER_STEP[mw.get(head_name).block] * args.steps,
             "clocks": head.get("clocks"),

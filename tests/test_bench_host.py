@@ -93,3 +93,10 @@ def test_targets_of():
                                                                            "layer_roofline_frac": 0.55}}
     t = bench.targets_of(res)
     assert t["decode"]["met"] and not t["block"]["met"] and "skewed" not in t
+
+
+def test_fraction_of_nominal_peaks():
+    """Fractions against the nominal B300 figures: GB/s over 8000 for an
+    HBM-bound kernel, TFLOP/s over 2250 for a tensor-bound one."""
+    assert bench.of_nominal("hbm", 6000.0) == 6000.0 / 8000.0
+    assert bench.of_nominal("tensor", 1500.0) == 1500.0 / 2250.0
