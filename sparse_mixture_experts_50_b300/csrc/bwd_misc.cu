@@ -118,29 +118,75 @@ __global__ void __launch_bounds__(256) dx_gather_kernel(const __nv_bfloat16* __r
 }
 
 // ---------------------------------------------------------------- dWg
-// Block (column block of 256, token chunk): per-expert sums of dl * x for its
-// columns over its tokens, in shared memory (each thread owns a column).
-__global__ void __launch_bounds__(256) dwg_partial_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          const int32_t* __restrict__ idx,
-                                                          const float* __restrict__ dl, float* __restrict__ part,
-                                                          int T, int d, int E, int k, int chunk) {
-  extern __shared__ float accs[];  // [E][256]
+// dWg = G^T x with G[t, e] = sum_j [i[t,j] = e] dl[t,j]: a [T, E] matrix with
+// k nonzeros per row, so a small dense contraction over the tokens.  A block
+// takes a chunk of tokens and 2048 columns; each thread owns 8 consecutive
+// columns (one 16-byte load of x per token) and keeps 8 experts x 8 columns
+// of fp32 sums in registers (experts in groups of 8).  The chunk's G rows
+// are built in shared memory, kDwgSub tokens at a time, one thread per token
+// adding its k entries in slot order.  Every sum runs in token order, and
+// the chunks' partial sums are added in chunk order: the result does not
+// depend on the launch shape's timing.
+constexpr int kDwgThreads = 256;
+constexpr int kDwgCols = 8;
+constexpr int kDwgGroup = 8;
+constexpr int kDwgSub = 64;
+
+__global__ void __launch_bounds__(kDwgThreads) dwg_partial_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                  const int32_t* __restrict__ idx,
+                                                                  const float* __restrict__ dl,
+                                                                  float* __restrict__ part, int T, int d, int E, int k,
+                                                                  int chunk) {
+  extern __shared__ float G[];  // [kDwgSub][E]
   pdl_enter();
-  const int c = blockIdx.x * 256 + threadIdx.x;
   const int t0 = blockIdx.y * chunk;
   const int t1 = min(T, t0 + chunk);
-  for (int e = 0; e < E; ++e) accs[e * 256 + threadIdx.x] = 0.0f;
-  if (c < d) {
-    for (int t = t0; t < t1; ++t) {
-      const float xv = __bfloat162float(x[static_cast<size_t>(t) * d + c]);
-      for (int j = 0; j < k; ++j) {
-        const size_t f = static_cast<size_t>(t) * k + j;
-        const int e = idx[f];
-        if (e >= 0 && e < E) accs[e * 256 + threadIdx.x] = fmaf(dl[f], xv, accs[e * 256 + threadIdx.x]);
+  const int c0 = (blockIdx.x * kDwgThreads + threadIdx.x) * kDwgCols;
+  const bool live = c0 < d;
+  for (int eg = 0; eg < E; eg += kDwgGroup) {
+    float acc[kDwgGroup][kDwgCols];
+#pragma unroll
+    for (int e = 0; e < kDwgGroup; ++e)
+#pragma unroll
+      for (int q = 0; q < kDwgCols; ++q) acc[e][q] = 0.0f;
+    for (int s0 = t0; s0 < t1; s0 += kDwgSub) {
+      const int ns = min(kDwgSub, t1 - s0);
+      __syncthreads();  // the previous sub-chunk's G is no longer read
+      for (int i = threadIdx.x; i < kDwgSub * E; i += kDwgThreads) G[i] = 0.0f;
+      __syncthreads();
+      for (int t = threadIdx.x; t < ns; t += kDwgThreads) {
+        for (int j = 0; j < k; ++j) {
+          const size_t f = static_cast<size_t>(s0 + t) * k + j;
+          const int e = __ldg(idx + f);
+          if (e >= 0 && e < E) G[t * E + e] += __ldg(dl + f);
+        }
+      }
+      __syncthreads();
+      if (live) {
+#pragma unroll 4
+        for (int t = 0; t < ns; ++t) {
+          float xv[kDwgCols];
+          load_vec(x + static_cast<size_t>(s0 + t) * d + c0, xv);
+#pragma unroll
+          for (int e = 0; e < kDwgGroup; ++e) {
+            const float g = eg + e < E ? G[t * E + eg + e] : 0.0f;
+#pragma unroll
+            for (int q = 0; q < kDwgCols; ++q) acc[e][q] = fmaf(g, xv[q], acc[e][q]);
+          }
+        }
       }
     }
-    for (int e = 0; e < E; ++e)
-      part[(static_cast<size_t>(blockIdx.y) * E + e) * d + c] = accs[e * 256 + threadIdx.x];
+    if (live) {
+#pragma unroll
+      for (int e = 0; e < kDwgGroup; ++e) {
+        if (eg + e >= E) break;
+        float* dst = part + (static_cast<size_t>(blockIdx.y) * E + eg + e) * d + c0;
+        const float lo[4] = {acc[e][0], acc[e][1], acc[e][2], acc[e][3]};
+        const float hi[4] = {acc[e][4], acc[e][5], acc[e][6], acc[e][7]};
+        store_vec(dst, lo);
+        store_vec(dst + 4, hi);
+      }
+    }
   }
 }
 
@@ -177,20 +223,18 @@ cudaError_t launch_dx_gather(const void* dx_perm, const int32_t* slot_pos, const
   return cudaGetLastError();
 }
 
-int dwg_chunks(int T) { return T < 64 ? 1 : (T + 255) / 256 < 64 ? (T + 255) / 256 : 64; }
+// Token chunks of dWg's first stage: ~64 tokens each, at most 64 chunks.
+int dwg_chunks(int T) { return T <= 64 ? 1 : (T + 63) / 64 < 64 ? (T + 63) / 64 : 64; }
 
 cudaError_t launch_dwg(const void* x, const int32_t* idx, const float* dl, float* part, float* dWg, int T, int d, int E,
                        int k, const Ctx& c, cudaStream_t s) {
   const int nch = dwg_chunks(T);
   const int chunk = (T + nch - 1) / nch;
-  dim3 grid((d + 255) / 256, nch);
-  const size_t smem = static_cast<size_t>(E) * 256 * sizeof(float);
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(dwg_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-          cudaSuccess)
-    return cudaGetLastError();
-  launch_pdl(dwg_partial_kernel, grid, dim3(256), smem, s, static_cast<const __nv_bfloat16*>(x), idx, dl, part, T, d,
-             E, k, chunk);
+  const int cols_per_block = kDwgThreads * kDwgCols;
+  dim3 grid((d + cols_per_block - 1) / cols_per_block, nch);
+  const size_t smem = static_cast<size_t>(kDwgSub) * E * sizeof(float);  // <= 16 KB (E <= 64)
+  launch_pdl(dwg_partial_kernel, grid, dim3(kDwgThreads), smem, s, static_cast<const __nv_bfloat16*>(x), idx, dl, part,
+             T, d, E, k, chunk);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int Ed = E * d;
