@@ -559,6 +559,74 @@ def config_of(name, n_gpus):
             "l2": "flushed between timed steps (256 MiB write); expert weights (2.8 GB) also exceed L2"}
 
 
+def ep_leg(args, name, world, rank, local):
+    """The expert-parallel form of the layer (ExpertParallelMoE over NCCL):
+    each of the `world` ranks holds E/world experts and its own batch of the
+    workload's shape, and routes, exchanges, runs its experts and combines
+    every step.  Host-clock timed (each step brings the exchange's counts to
+    the host), barrier and device synchronise on both sides, slowest rank."""
+    import torch.distributed as dist
+    from sparse_mixture_experts_50_b300.expert_parallel import ExpertParallelMoE, TorchComm
+    wl = mw.get(name)
+    if wl.w8 or wl.bwd or wl.block or wl.dtype != "bf16" or wl.E % world:
+        raise SystemExit(f"--expert-parallel runs a plain bf16 forward workload with E divisible by {world}")
+    device = f"cuda:{local}"
+    t = mw.make_inputs(wl, x_seed=1000 + rank)
+    El = wl.E // world
+    mine = slice(rank * El, (rank + 1) * El)
+    g = {"x": t["x"].to(device), "Wg": t["Wg"].to(device)}
+    for n in ("W1", "W3", "W2"):
+        g[n] = t[n][mine].contiguous().to(device)
+    del t
+    layer = ExpertParallelMoE(g["Wg"], g["W1"], g["W3"], g["W2"], wl.k, TorchComm())
+    for _ in range(args.warmup):
+        layer.forward(g["x"])
+    if layer.B.moe_get_device_status(reset=True) != 0:
+        raise RuntimeError("expert-parallel: device status after the warm-up steps")
+    clocks = ClockSampler(local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        layer.forward(g["x"])
+    torch.cuda.synchronize()
+    dist.barrier()
+    el = time.perf_counter() - t0
+    clk = clocks.stop()
+    value, t_max = job_throughput(wl.T * args.steps, el, True, device)
+    ms = t_max / args.steps * 1e3
+    peaks = load_peaks()
+    # Each rank streams its own experts' weights once per step (decode: all of them are used).
+    local_bytes = El * 3 * wl.d * wl.F * 2
+    achieved = local_bytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**config_of(name, world),
+                   "parallelism": f"expert-parallel x{world}: {El} experts per rank, NCCL all-to-all of counts and rows",
+                   "l2": "not flushed (each step's exchange synchronises with the host)"},
+        "impl": "native",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "whole expert-parallel step (this rank's expert weights per step time)"},
+        "e2e": None, "cpu_baseline": None,
+        "gpu_launches": 7 * args.steps,
+        "clocks": clk,
+    }
+
+
+def flush_c_stdio():
+    """Flush the C library's stdout buffers (NCCL prints its version line
+    through them), so that the JSON line printed next stays the last line."""
+    try:
+        import ctypes
+        ctypes.CDLL(None).fflush(None)
+    except Exception:  # pragma: no cover
+        pass
+
+
 def ensure_built():
     from sparse_mixture_experts_50_b300 import binding
     if not os.path.exists(binding.LIB_PATH):
@@ -577,6 +645,9 @@ def main():
                     help="workload of the JSON line's value (default: Mixtral-shape decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--expert-parallel", action="store_true",
+                    help="time the expert-parallel layer (E/N experts per rank, NCCL all-to-alls) on the headline "
+                         "workload instead of the replica bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -616,6 +687,24 @@ def main():
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "wall_s": time.perf_counter() - t0}
         print(json.dumps(line), flush=True)
+        return
+
+    if args.expert_parallel:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU for the native implementation")
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", str(29600 + os.getpid() % 1000))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", rank=rank, world_size=world, device_id=torch.device(f"cuda:{local}"))
+        try:
+            ensure_built()
+            line = ep_leg(args, head_name, world, rank, local)
+            if rank == 0:
+                flush_c_stdio()
+                print(json.dumps(line), flush=True)
+        finally:
+            dist.destroy_process_group()
         return
 
     dist_on = world > 1
@@ -682,6 +771,7 @@ def main():
             "workloads": {n: {**{k: v for k, v in r.items() if k != "clocks"},
                               "sm_mhz": (r.get("clocks") or {}).get("sm_mhz")} for n, r in results.items()},
         }
+        flush_c_stdio()
         print(json.dumps(line), flush=True)
     if dist_on:
         torch.distributed.barrier()

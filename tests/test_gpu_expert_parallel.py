@@ -1,12 +1,14 @@
-"""The expert-parallel layer's GPU steps on one GPU, with the ranks emulated
-in one process (GPU).
+"""The expert-parallel layer's GPU steps on one GPU (GPU).
 
-Two (or four) ranks' routing, experts and combine run through the
-library's kernels one rank after another; the exchanges between them are
-done here by slicing and concatenating the blocks each rank sends, in the
-order torch.distributed's all-to-all would deliver them.  Each rank's output
-must match the single-GPU layer's on its own tokens and the oracle.  (The
-exchange itself over torch.distributed is covered on CPU ranks with gloo.)
+Two (or four) ranks are emulated in one process: their routing, experts and
+combine run through the library's kernels one rank after another, and the
+exchanges between them are done here by slicing and concatenating the
+blocks each rank sends, in the order torch.distributed's all-to-all would
+deliver them.  Each rank's output must match the single-GPU layer's on its
+own tokens and the oracle.  The layer's own forward also runs over NCCL
+with one rank (the all-to-alls are then the identity), and so does the
+bench's expert-parallel leg.  The exchange between several ranks over
+torch.distributed is covered on CPU ranks with gloo.
 """
 import numpy as np
 import pytest
@@ -133,3 +135,24 @@ def test_expert_parallel_forward_over_nccl_one_rank(B):
     assert p.exitcode == 0
     same, status = q.get(timeout=5)
     assert status == 0 and same
+
+
+def test_bench_expert_parallel_leg_one_rank(B):
+    """bench.py --expert-parallel at one rank (NCCL world of one): the leg
+    runs the Mixtral-shape decode through ExpertParallelMoE and prints one
+    well-formed JSON line."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--expert-parallel", "--steps", "3",
+                        "--warmup", "3"], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = r.stdout.strip().splitlines()
+    assert lines and lines[-1].startswith("{"), r.stdout[-500:]
+    line = json.loads(lines[-1])
+    assert line["n_gpus"] == 1 and line["steps"] == 3 and line["value"] > 0
+    assert line["config"]["parallelism"].startswith("expert-parallel x1")
+    assert line["roofline"]["bound"] == "hbm" and line["roofline"]["achieved"] > 0
