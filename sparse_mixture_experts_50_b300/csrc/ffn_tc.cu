@@ -11,7 +11,9 @@
 //               (M=128, N=256, K=16, bf16 in, fp32 accumulate) into one of
 //               two 256-column accumulators.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator rows, fp32 math,
-//               bf16 rounding, stores of the rows that belong to the expert.
+//               bf16 rounding, stores of the rows that belong to the expert
+//               (large batches: 32 x 32 blocks staged through shared memory,
+//               so that each store instruction writes whole row segments).
 // Output tiles are 128 rows of one expert's segment x (gate/up) 128 columns
 // of h, whose accumulator holds the W1 half in columns 0-127 and the W3 half
 // in 128-255, or (down) 256 columns of y.  Tiles are numbered expert by
@@ -151,7 +153,10 @@ struct Plan {
   static_assert(tok_stages <= 8, "token ring too deep");
   static constexpr size_t ring_bytes = static_cast<size_t>(stages) * stage_bytes +
                                        static_cast<size_t>(tok_stages) * a_bytes;
-  static constexpr size_t smem_bytes = 1024 + ring_bytes + sizeof(SmemCtl);
+  static constexpr size_t ctl_bytes = (sizeof(SmemCtl) + 127) / 128 * 128;
+  // Large-batch mode: one 32 x 64-byte staging block per epilogue warp.
+  static constexpr size_t stg_bytes = SWAP ? 0 : 4 * 32 * 64;
+  static constexpr size_t smem_bytes = 1024 + ring_bytes + ctl_bytes + stg_bytes;
   static_assert(stages <= MAX_STAGES, "too many stages");
   static_assert(smem_bytes <= 227 * 1024, "plan exceeds shared memory");
   static_assert(2 * acc_cols <= tmem_cols, "accumulators exceed the tensor-memory allocation");
@@ -232,6 +237,29 @@ __device__ __forceinline__ void prefetch_first_tile(const GemmArgs& args, int la
     if (r < args.b_rows)
       ptx::prefetch_l2_bulk(base + (static_cast<size_t>(e) * args.b_rows + r) * row_bytes, bytes);
   }
+}
+
+// The warp's 32 rows x 32 bf16 columns (lane = row, pk[i] = columns 2i, 2i+1)
+// to dst[r * ld + ...] for r < rows.  Each lane writes its 64-byte row into
+// the warp's staging block as four 16-byte units (unit j of row r at unit
+// j ^ ((r >> 1) & 3), so that a quarter-warp meets distinct banks); then every
+// load/store instruction moves eight whole 64-byte rows, four lanes per row,
+// instead of touching 32 rows at once.
+__device__ __forceinline__ void warp_store_rows_bf16(uint32_t stg, const uint32_t (&pk)[16], __nv_bfloat16* dst,
+                                                     size_t ld, int rows, int lane) {
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    ptx::sts128(stg + lane * 64 + ((j ^ sw) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+  __syncwarp();
+  const int sub = lane >> 2, u = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + sub;
+    const uint4 val = ptx::lds128(stg + r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+    if (r < rows) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * ld + 8 * u) = val;
+  }
+  __syncwarp();
 }
 
 // What the training forward keeps for the backward of h = silu(a) b, formed
@@ -465,8 +493,6 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int e, m, n;
       decode_tile(ctl, args.E, tile, e, m, n);
-      const int grow = ctl->seg[e] + m * ROWS + row_in_tile;
-      const bool row_ok = grow < ctl->seg[e + 1];
       // tcgen05.ld below is warp-collective: leave together or not at all.
       const bool ready = ptx::mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag, args.wait_ns);
       if (!__all_sync(0xFFFFFFFFu, ready)) {
@@ -515,13 +541,16 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
         }
       } else if (SWIGLU) {
         const int col0 = n * BN_HALF;
+        const int wrow0 = ctl->seg[e] + m * ROWS + quad * 32;  // the warp's first row
+        const int wrows = max(0, min(32, ctl->seg[e + 1] - wrow0));
+        const uint32_t stg = ptx::smem_u32(smem + P::ring_bytes + P::ctl_bytes) + quad * 32 * 64;
 #pragma unroll 1
         for (int c = 0; c < BN_HALF; c += 32) {
           uint32_t g[32], u[32];
           ptx::tmem_ld_32x32b_x32(t_row + c, g);
           ptx::tmem_ld_32x32b_x32(t_row + BN_HALF + c, u);
           ptx::tmem_ld_wait();
-          if (row_ok && col0 + c < args.n_out) {
+          if (col0 + c < args.n_out) {
             const size_t srow = static_cast<size_t>(e) * args.b_rows + col0 + c;
             uint32_t pk[16];
 #pragma unroll
@@ -550,29 +579,32 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
                 u[i] = pack_bf16x2(q0, q1);
               }
             }
-            uint4* dst = reinterpret_cast<uint4*>(args.out + static_cast<size_t>(grow) * args.ldo + col0 + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            const size_t o = static_cast<size_t>(wrow0) * args.ldo + col0 + c;
+            warp_store_rows_bf16(stg, pk, args.out + o, args.ldo, wrows, lane);
             if (!W8 && args.keep != nullptr) {
-              const size_t o = static_cast<size_t>(grow) * args.ldo + col0 + c;
-              uint4* dp = reinterpret_cast<uint4*>(args.keep + o);
-              uint4* dq = reinterpret_cast<uint4*>(args.keep + static_cast<size_t>(args.Tk) * args.ldo + o);
+              uint32_t pp[16], qq[16];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                dp[q] = make_uint4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
-                dq[q] = make_uint4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+              for (int i = 0; i < 16; ++i) {
+                pp[i] = g[i];
+                qq[i] = u[i];
               }
+              warp_store_rows_bf16(stg, pp, args.keep + o, args.ldo, wrows, lane);
+              warp_store_rows_bf16(stg, qq, args.keep + static_cast<size_t>(args.Tk) * args.ldo + o, args.ldo, wrows,
+                                   lane);
             }
           }
         }
       } else {
         const int col0 = n * BN;
+        const int wrow0 = ctl->seg[e] + m * ROWS + quad * 32;  // the warp's first row
+        const int wrows = max(0, min(32, ctl->seg[e + 1] - wrow0));
+        const uint32_t stg = ptx::smem_u32(smem + P::ring_bytes + P::ctl_bytes) + quad * 32 * 64;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(t_row + c, v);
           ptx::tmem_ld_wait();
-          if (row_ok && col0 + c < args.n_out) {
+          if (col0 + c < args.n_out) {
             const size_t srow = static_cast<size_t>(e) * args.b_rows + col0 + c;
             uint32_t pk[16];
 #pragma unroll
@@ -585,9 +617,8 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
               }
               pk[i] = pack_bf16x2(y0, y1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(args.out + static_cast<size_t>(grow) * args.ldo + col0 + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            warp_store_rows_bf16(stg, pk, args.out + static_cast<size_t>(wrow0) * args.ldo + col0 + c, args.ldo, wrows,
+                                 lane);
           }
         }
       }
