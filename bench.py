@@ -612,7 +612,8 @@ def ep_leg(args, name, world, rank, local):
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                      "kernel": "whole expert-parallel step (this rank's expert weights per step time)"},
         "e2e": None, "cpu_baseline": None,
-        "gpu_launches": 7 * args.steps,
+        # router, dispatch + row copy, regroup, gate/up + down, ungroup, combine
+        "gpu_launches": 8 * args.steps,
         "clocks": clk,
     }
 
