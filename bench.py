@@ -261,6 +261,13 @@ def make_tensors(wl, shared):
 
 
 def time_layer(layer, steps, warmup, flush, dist_on):
+    """K timed steps, each bracketed by CUDA events on the launching stream
+    (an L2 flush between steps, outside the events), then K more steps with
+    events recorded inside the call between its kernels, for the per-kernel
+    split.  Only the first pass gives the step time: an event recorded between
+    two kernels ends the overlap of the second kernel's launch and set-up with
+    the first's tail (programmatic dependent launch)."""
+    outer = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     for _ in range(warmup):
         layer.step()
@@ -271,14 +278,20 @@ def time_layer(layer, steps, warmup, flush, dist_on):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
-        layer.step(evs[i])
+        outer[i][0].record()
+        layer.step()
+        outer[i][1].record()
         flush.zero_()
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     if dist_on:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    step_ms = [a.elapsed_time(b) for a, b in outer]
+    for i in range(steps):
+        layer.step(evs[i])
+        flush.zero_()
+    torch.cuda.synchronize()
     parts = {
         "router_dispatch": [e[0].elapsed_time(e[1]) for e in evs],
         "gate_up": [e[1].elapsed_time(e[2]) for e in evs],
