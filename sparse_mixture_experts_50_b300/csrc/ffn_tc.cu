@@ -42,7 +42,11 @@
 // memory, whose bandwidth would otherwise bound the small-batch int8 GEMM.
 // The converters are two groups of four warps taking alternate K steps: a
 // group's step is a chain of shared-memory loads, widening, tensor-memory
-// stores and their wait, and two groups overlap those chains.
+// stores and their wait, and two groups overlap those chains.  At N=32 one
+// thread issues an MMA every ~48 cycles whatever it feeds, four times the
+// tensor pipe's time for it, so the int8 form issues from two threads, one
+// per 128-row half (its own accumulator): 16 MMAs per 128-K stage would
+// otherwise take longer to issue than the stage takes to stream.
 //
 // Every wait is bounded (globaltimer + iteration cap).  A wait that runs out
 // raises a CTA-wide abort flag and records MOE_ETIMEOUT; each role then
@@ -144,8 +148,10 @@ struct Plan {
   static constexpr int tok_stages = tmem_a ? MOE_TOK_STAGES : 0;  // separate token ring
   static constexpr int conv_warps = W8 ? CONV_WARPS * CONV_GROUPS : 0;  // from warp 6
   static constexpr int tok_warp = 6 + conv_warps;        // the token ring's producer (int8)
+  static constexpr int issuers = tmem_a ? 2 : 1;         // MMA-issuing threads, one per 128-row half
+  static constexpr int mma2_warp = tok_warp + 1;         // the second issuer's warp (int8)
   static constexpr int stages = SWAP ? (W8 ? MOE_W8_SWAP_STAGES : MOE_SWAP_STAGES) : 4;
-  static constexpr int threads = 192 + 32 * conv_warps + (tmem_a ? 32 : 0);
+  static constexpr int threads = 192 + 32 * conv_warps + (tmem_a ? 64 : 0);
   static constexpr int acc_cols = SWAP ? 2 * TN : BN;    // fp32 columns of one accumulator
   static constexpr int tmem_cols = (SWAP && !W8) ? 128 : 512;  // power of two
   static_assert(!tmem_a || TMEM_A_COL0 + TMEM_A_STAGES * TMEM_A_STAGE_COLS <= 512, "tensor-memory ring too deep");
@@ -298,19 +304,20 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
       ptx::mbar_init(&ctl->full[s], 1);
       ptx::mbar_init(&ctl->empty[s], W8 ? CONV_WARPS : 1);
     }
+    // Barriers the MMAs complete get one arrival per issuing thread.
     for (int s = 0; s < P::tok_stages; ++s) {
       ptx::mbar_init(&ctl->tok_full[s], 1);
-      ptx::mbar_init(&ctl->tok_empty[s], 1);
+      ptx::mbar_init(&ctl->tok_empty[s], P::issuers);
     }
     for (int s = 0; s < (W8 ? TMEM_A_STAGES : 0); ++s) {
       ptx::mbar_init(&ctl->c_full[s], CONV_WARPS);
-      ptx::mbar_init(&ctl->c_empty[s], 1);
+      ptx::mbar_init(&ctl->c_empty[s], P::issuers);
     }
     for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(&ctl->tfull[a], 1);
+      ptx::mbar_init(&ctl->tfull[a], P::issuers);
       ptx::mbar_init(&ctl->tempty[a], EPI_THREADS);
     }
-    ptx::mbar_init(&ctl->drain, 1);
+    ptx::mbar_init(&ctl->drain, P::issuers);
     ctl->abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -407,9 +414,11 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
         if (filled & (1u << s)) ptx::mbar_wait(&ctl->full[s], last_parity[s], nullptr, drain_limit(args.wait_ns));
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (P::issuers > 1 && warp == P::mma2_warp)) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
+      // int8: thread `half` issues the MMAs of its 128-row half only.
+      const int half = warp == 1 ? 0 : 1;
       int stage = 0, cstage = 0;
       uint32_t phase = 0, cphase = 0;
       int acc = 0;
@@ -436,24 +445,35 @@ __global__ void __launch_bounds__(Plan<W8, SWAP>::threads, 1)
           const uint32_t sa = P::tmem_a ? ptx::smem_u32(toks + stage * AB) : ptx::smem_u32(smem + stage * SB);
           const uint32_t sb = sa + AB;
           const uint32_t ta = tmem_base + TMEM_A_COL0 + static_cast<uint32_t>(cstage * TMEM_A_STAGE_COLS);
+          if (SWAP) {
+            // Small-batch forms: the operands' bases once per stage, constant
+            // offsets per K step (descriptor start addresses count 16 bytes).
+            const uint64_t tdesc0 = ptx::sdesc_kmajor_sw128(sa);
+            const uint32_t acc0 = kb > 0 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < P::kstep / UMMA_K; ++kk) {
-            const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
-            // token operand: 64-wide box kk / 4, K offset (kk % 4) * 16 within it
-            const uint64_t tdesc = ptx::sdesc_kmajor_sw128(sa + (kk / (BK / UMMA_K)) * P::tok_box_bytes +
-                                                           (kk % (BK / UMMA_K)) * UMMA_K * 2);
-            if (P::tmem_a) {
-              // widened weights (two 128-lane halves in tensor memory) x the 32-token tile
-              ptx::umma_bf16_tmem_a(d_tmem, ta + kk * (UMMA_K / 2), tdesc, IDESC_SWAP, acc_flag);
-              ptx::umma_bf16_tmem_a(d_tmem + TN, ta + TMEM_A_HALF_COLS + kk * (UMMA_K / 2), tdesc, IDESC_SWAP,
-                                    acc_flag);
-            } else if (SWAP) {
-              // weights (two 128-row halves) x the 32-token tile
-              const uint64_t w0 = ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2);
-              const uint64_t w1 = ptx::sdesc_kmajor_sw128(sb + B_HALF_BYTES + kk * UMMA_K * 2);
-              ptx::umma_bf16(d_tmem, w0, tdesc, IDESC_SWAP, acc_flag);
-              ptx::umma_bf16(d_tmem + TN, w1, tdesc, IDESC_SWAP, acc_flag);
-            } else {
+            for (int kk = 0; kk < P::kstep / UMMA_K; ++kk) {
+              const uint32_t f = kk == 0 ? acc0 : 1u;
+              // token operand: 64-wide box kk / 4, K offset (kk % 4) * 16 within it
+              const uint64_t tdesc = tdesc0 + static_cast<uint64_t>(((kk / (BK / UMMA_K)) * P::tok_box_bytes +
+                                                                      (kk % (BK / UMMA_K)) * UMMA_K * 2) >> 4);
+              if (P::tmem_a) {
+                // widened weights of this thread's half (128 lanes of tensor memory) x the 32-token tile
+                ptx::umma_bf16_tmem_a(d_tmem + half * TN, ta + half * TMEM_A_HALF_COLS + kk * (UMMA_K / 2), tdesc,
+                                      IDESC_SWAP, f);
+              } else {
+                // weights (two 128-row halves) x the 32-token tile
+                const uint64_t w0 = ptx::sdesc_kmajor_sw128(sb) + static_cast<uint64_t>((kk * UMMA_K * 2) >> 4);
+                const uint64_t w1 = w0 + static_cast<uint64_t>(B_HALF_BYTES >> 4);
+                ptx::umma_bf16(d_tmem, w0, tdesc, IDESC_SWAP, f);
+                ptx::umma_bf16(d_tmem + TN, w1, tdesc, IDESC_SWAP, f);
+              }
+            }
+          } else {
+            // Large batches: the 128-row token tile x 256 weight rows.
+#pragma unroll
+            for (int kk = 0; kk < P::kstep / UMMA_K; ++kk) {
+              const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
+              const uint64_t tdesc = ptx::sdesc_kmajor_sw128(sa + kk * UMMA_K * 2);
               const uint64_t bdesc = ptx::sdesc_kmajor_sw128(sb + kk * UMMA_K * 2);
               ptx::umma_bf16(d_tmem, tdesc, bdesc, IDESC, acc_flag);
             }
