@@ -34,7 +34,7 @@ def test_header_declares_the_layer_steps():
 
 # The boundary the layer's scope table names, with each call's argument count
 # (pointers, sizes, dtype and stream, in that table's order).
-SURVEY_BOUNDARY = {
+BOUNDARY_CALLS = {
     "moe_router_topk": 11,       # x, Wg, T, d, E, k, topk_idx, topk_w, logits_opt, dtype, stream
     "moe_permute": 13,           # x, topk_idx, T, d, E, k, counts, offsets, row_src, slot_pos, x_perm, dtype, stream
     "moe_expert_ffn": 12,        # x_perm, offsets, W1, W3, W2, y_perm, Tk, d, dff, E, dtype, stream
@@ -48,7 +48,7 @@ SURVEY_BOUNDARY = {
 
 def test_boundary_names_and_arities():
     names = declared_functions()
-    for n, nargs in SURVEY_BOUNDARY.items():
+    for n, nargs in BOUNDARY_CALLS.items():
         assert n in names, f"include/moe.h does not declare {n}"
         assert len(B.SIGNATURES[n][1]) == nargs, (n, len(B.SIGNATURES[n][1]), nargs)
     assert B.SIGNATURES["moe_workspace_bytes"][0] is ctypes.c_size_t
