@@ -32,8 +32,8 @@ def test_header_declares_the_layer_steps():
         assert n in names
 
 
-# The boundary the layer's scope table names, with each call's argument count
-# (pointers, sizes, dtype and stream, in that table's order).
+# The layer's boundary calls, with each call's argument count
+# (pointers, sizes, dtype and stream, in the header's order).
 BOUNDARY_CALLS = {
     "moe_router_topk": 11,       # x, Wg, T, d, E, k, topk_idx, topk_w, logits_opt, dtype, stream
     "moe_permute": 13,           # x, topk_idx, T, d, E, k, counts, offsets, row_src, slot_pos, x_perm, dtype, stream
