@@ -89,8 +89,9 @@ def test_quantize_bit_exact(B, shape):
 
 # ------------------------------------------------------------------ experts
 @pytest.mark.parametrize("counts", [
-    [0, 128, 129, 1, 0, 255, 256, 300],  # wide tiles: 192-token edges, empty experts
-    [191, 192, 193, 0, 384, 385, 1, 0],   # wide tiles: one short of, at and past 192-token edges
+    [0, 128, 129, 1, 0, 255, 256, 300],  # wide tiles, empty experts
+    [191, 192, 193, 0, 384, 385, 1, 0],   # wide tiles: uneven counts
+    [223, 224, 225, 0, 448, 449, 1, 0],   # wide tiles: one short of, at and past 224-token edges
     [1000, 0, 0, 0, 0, 0, 0, 0],          # every row in one expert
     [0, 0, 0, 0, 0, 0, 0, 129],           # just past the small-batch limit, last expert only
     [3, 1, 4, 1, 5, 9, 2, 6],             # decode-like: a few rows each
@@ -99,7 +100,7 @@ def test_quantize_bit_exact(B, shape):
 ])
 def test_expert_w8_tiles(B, counts):
     """The int8 grouped GEMMs on hand-made segments: up to 128 rows the
-    small-batch form, beyond it the wide form (192 tokens per tile); d is not
+    small-batch form, beyond it the wide form (224 tokens per tile); d is not
     a multiple of the 128-row weight blocks of the wide down GEMM, nor d_ff
     of the 256-column tiles."""
     r = np.random.default_rng(sum(counts) + 1)
