@@ -139,7 +139,7 @@ int launch_w8_gate_up(const void* x_perm, const int32_t* offsets, const int8_t* 
 int launch_w8_down(const void* h, const int32_t* offsets, const int8_t* W2q, const float* W2s, void* y,
                    int Tk, int d, int dff, int E, const Ctx& c, cudaStream_t s);
 // The same products beyond the small-batch case: weights widened into tensor
-// memory as the MMA's A operand, 192 tokens per tile (ffn_w8_wide.cu).
+// memory as the MMA's A operand, 224 tokens per tile (ffn_w8_wide.cu).
 int launch_w8_wide_gate_up(const void* x_perm, const int32_t* offsets, const int8_t* W1q, const float* W1s,
                            const int8_t* W3q, const float* W3s, void* h, int Tk, int d, int dff, int E,
                            const Ctx& c, cudaStream_t s);
