@@ -54,18 +54,22 @@ def test_wait_timeout_is_reported_and_context_survives():
 def test_small_batch_wait_timeout(w8):
     """Decode-sized GEMMs (32 routed rows over 8 experts, one empty): a 1 ns
     limit ends both GEMMs with MOE_ETIMEOUT, and the next calls with the
-    default limit give the same bits as the calls made before it."""
+    default limit give the same bits as the calls made before it.  K is
+    long (d=4096, dff=2048: 32-64 weight stages per tile), so the epilogue's
+    wait for its first accumulator outlasts any suspension of a barrier
+    try-wait and has to spin; with K=512 a whole launch could finish inside
+    the first try-waits and report no timeout."""
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     from sparse_mixture_experts_50_b300 import binding as B
-    r = np.random.default_rng(3)
-    E, d, F = 8, 512, 1024
+    E, d, F = 8, 4096, 2048
     counts = [5, 5, 6, 0, 2, 7, 3, 4]
     offsets = np.concatenate([[0], np.cumsum(counts)])
     Tk = int(offsets[-1])
-    x = torch.from_numpy(r.standard_normal((Tk, d))).to(torch.bfloat16).cuda()
-    W1, W3 = (torch.from_numpy(r.standard_normal((E, F, d)) * 0.05).to(torch.bfloat16).cuda() for _ in range(2))
-    W2 = torch.from_numpy(r.standard_normal((E, d, F)) * 0.05).to(torch.bfloat16).cuda()
+    g = torch.Generator(device="cuda").manual_seed(3)
+    x = torch.randn(Tk, d, device="cuda", generator=g).to(torch.bfloat16)
+    W1, W3 = ((torch.randn(E, F, d, device="cuda", generator=g) * 0.02).to(torch.bfloat16) for _ in range(2))
+    W2 = (torch.randn(E, d, F, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
     off = torch.from_numpy(offsets).int().cuda()
     B.moe_get_device_status(reset=True)
     if w8:
